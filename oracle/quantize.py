@@ -1,0 +1,236 @@
+"""Quantizers of the hot path: amax, per-tensor FP8, MXFP8, NVFP4 (+RHT, SR).
+
+Test infrastructure (see ``oracle/__init__``).
+
+Conventions
+  * A tensor X is [R, C] row-major; its contraction dimension for the row copy
+    is C.  The "row copy" quantizes X with blocks along C; the "col copy"
+    quantizes X^T ([C, R]) with blocks along R.  Fprop/Dgrad read row copies,
+    Wgrad reads col copies (blocks along the token dimension M).
+  * Inputs arrive as float32 arrays (bf16 inputs widened exactly).
+  * Every operation that decides a code is fp32 round-to-nearest-even.
+
+Sources.  Per-tensor scaling of each weight / activation tensor and its
+refresh every step: "Introduction to FP8 training using Transformer Engine",
+section "FP8 Training について".  The per-tensor amax needs an extra memory pass,
+and NVFP4 adds a random Hadamard transform on the Wgrad inputs, stochastic
+rounding of gradients and 2D block scaling of weights: "How to Optimize
+Transformer-Based Models for Low-Precision Training", section
+"実モデルにおける結果の解釈" (list of NVFP4 overheads).  Block formats follow the
+public OCP Microscaling v1.0 (MXFP8: 32 elements, E8M0 scale
+2**(floor(log2 amax) - 8), E4M3 elements) and NVIDIA's NVFP4 format (16
+elements, E2M1 elements, UE4M3 block scale, fp32 tensor scale chosen so that
+the largest block scale is 448: S_enc = 448*6/amax).
+
+Parity: every function pinned in tests/test_oracle_quantize.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats as F
+from .philox import element_words
+
+f32 = np.float32
+
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+
+
+# ---- amax --------------------------------------------------------------------
+
+def amax(x) -> np.float32:
+    """max |x| over the whole tensor (exact; -0 counts as 0)."""
+    x = np.asarray(x, dtype=np.float32)
+    if x.size == 0:
+        return f32(0.0)
+    return f32(np.max(np.abs(x)))
+
+
+# ---- per-tensor FP8 ------------------------------------------------------------
+
+def fp8_cast(x, scale, fmt: str) -> np.ndarray:
+    """q = enc_fmt(fl32(x * scale)), saturating."""
+    v = (np.asarray(x, dtype=np.float32) * f32(scale)).astype(np.float32)
+    return F.encode(v, fmt)
+
+
+def fp8_quantize(x, scale, fmt: str):
+    """Row copy [R, C], col copy [C, R] (same per-tensor scale), amax, scale_inv."""
+    x = np.asarray(x, dtype=np.float32)
+    q_row = fp8_cast(x, scale, fmt)
+    q_col = fp8_cast(np.ascontiguousarray(x.T), scale, fmt)
+    return q_row, q_col, amax(x), f32(f32(1.0) / f32(scale))
+
+
+def fp8_dequant(q, scale_inv, fmt: str) -> np.ndarray:
+    return F.decode(q, fmt) * float(scale_inv)
+
+
+# ---- MXFP8 -----------------------------------------------------------------------
+
+MX_BLOCK = 32
+
+
+def mx_scale_exponent(block_amax, fmt: str = "e4m3") -> np.ndarray:
+    """Shared exponent E = clamp(floor(log2 a_b) - emax_elem, -127, 127); a_b = 0 -> -127.
+
+    emax_elem is the exponent of the element format's largest normal (8 for E4M3,
+    15 for E5M2).
+    """
+    emax = {"e4m3": 8, "e5m2": 15}[fmt]
+    a = np.asarray(block_amax, dtype=np.float64)
+    safe = np.where(a > 0, a, 1.0)
+    e = F.floor_log2(safe) - emax
+    e = np.where(a > 0, e, -127)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def mxfp8_quantize(z, fmt: str = "e4m3"):
+    """Blocks of 32 along the last axis of z [R, C]: (codes [R, C], E8M0 bytes [R, C/32])."""
+    z = np.asarray(z, dtype=np.float32)
+    R, C = z.shape
+    assert C % MX_BLOCK == 0
+    blk = z.reshape(R, C // MX_BLOCK, MX_BLOCK)
+    a_b = np.max(np.abs(blk), axis=2)
+    E = mx_scale_exponent(a_b, fmt)
+    mult = np.exp2(-E.astype(np.float64)).astype(np.float32)       # exact power of two
+    v = (blk * mult[:, :, None]).astype(np.float32)
+    q = F.encode(v, fmt).reshape(R, C)
+    return q, (E + 127).astype(np.uint8)
+
+
+def mxfp8_dequant(q, s, fmt: str = "e4m3") -> np.ndarray:
+    q = np.asarray(q)
+    R, C = q.shape
+    val = F.decode(q, fmt).reshape(R, C // MX_BLOCK, MX_BLOCK)
+    return (val * F.decode_e8m0(s)[:, :, None]).reshape(R, C)
+
+
+# ---- random Hadamard transform (16 points) -----------------------------------------
+
+def rht16(z, signs: int) -> np.ndarray:
+    """y = 1/4 * H16 * D * x on consecutive chunks of 16 along the last axis.
+
+    H16 is the Sylvester Hadamard matrix (H[i, j] = (-1)**popcount(i & j));
+    D = diag(d_j) with d_j = -1 where bit j of ``signs`` is set.  Evaluation
+    order (fp32): sign flip, butterflies for h = 1, 2, 4, 8 mapping
+    (y_i, y_{i+h}) -> (y_i + y_{i+h}, y_i - y_{i+h}) for every i with i & h == 0,
+    then the exact scaling by 1/4.
+    """
+    z = np.asarray(z, dtype=np.float32)
+    shape = z.shape
+    assert shape[-1] % 16 == 0
+    y = z.reshape(-1, 16).copy()
+    for j in range(16):
+        if (signs >> j) & 1:
+            y[:, j] = -y[:, j]
+    for h in (1, 2, 4, 8):
+        for i in range(16):
+            if i & h:
+                continue
+            a = y[:, i].copy()
+            b = y[:, i + h].copy()
+            y[:, i] = a + b
+            y[:, i + h] = a - b
+    y = (y * f32(0.25)).astype(np.float32)
+    return y.reshape(shape)
+
+
+# ---- NVFP4 ----------------------------------------------------------------------
+
+NV_BLOCK = 16
+NV_SENC_NUM = 448.0 * 6.0   # 2688
+
+
+def nvfp4_global(tensor_amax):
+    """(S_enc, S_dec) = (fl32(2688 / A), fl32(1 / S_enc)); S_enc = 1 when A = 0 or the quotient overflows."""
+    A = f32(tensor_amax)
+    with np.errstate(divide="ignore", over="ignore"):
+        s = f32(f32(NV_SENC_NUM) / A) if A > 0 else f32(1.0)
+    if not np.isfinite(s):
+        s = f32(1.0)
+    return s, f32(f32(1.0) / s)
+
+
+def e2m1_round_stochastic(v, words) -> np.ndarray:
+    """Stochastic rounding of fp32 values v to E2M1 codes.
+
+    |v| >= 6 saturates to 6.  Otherwise lo is the largest E2M1 magnitude <= |v|,
+    hi the next one, and frac = (|v| - lo) / (hi - lo) (exact in fp32: the
+    difference is exact by Sterbenz or lo = 0, the spacing is a power of two).
+    The magnitude rounds up iff (word >> 8) * 2**-24 < frac.  The sign is kept.
+    """
+    v = np.asarray(v, dtype=np.float32)
+    a = np.abs(v)
+    idx = np.searchsorted(E2M1_GRID, a, side="right") - 1
+    idx = np.clip(idx, 0, 7)
+    lo = E2M1_GRID[idx]
+    hi = E2M1_GRID[np.minimum(idx + 1, 7)]
+    span = np.where(idx < 7, hi - lo, f32(1.0)).astype(np.float32)
+    frac = ((a - lo).astype(np.float32) / span).astype(np.float32)
+    k = (np.asarray(words, dtype=np.uint32) >> 8).astype(np.float64)
+    up = (k * 2.0 ** -24) < frac.astype(np.float64)
+    mag = np.where(a >= 6.0, f32(6.0), np.where(up & (idx < 7), hi, lo)).astype(np.float32)
+    signed = np.where(np.signbit(v), -mag, mag).astype(np.float32)
+    return F.encode(signed, "e2m1")
+
+
+def nvfp4_quantize(z, tensor_amax, block2d: bool = False, sr=None):
+    """Quantize z [R, C] to NVFP4 with blocks along the last axis.
+
+    Returns (codes [R, C] as E2M1 nibbles 0..15, scales [R, C/16] UE4M3 bytes,
+    S_dec).  ``block2d``: one scale per 16x16 tile of z (rows within a 16-row
+    group share it).  ``sr``: None for round-to-nearest, else a dict with
+    ``seed``, ``copy_id``, ``offset``, ``row0`` (index of z's first row within
+    the full copy) and ``cols`` (row length of the full copy) for the random
+    words of stochastic rounding.
+
+    Per block b: s_b = UE4M3(fl32(fl32(a_b / 6) * S_enc)); r = fl32(S_enc / dec(s_b))
+    (r = 0 when dec(s_b) = 0); q = E2M1(fl32(x * r)).
+    """
+    z = np.asarray(z, dtype=np.float32)
+    R, C = z.shape
+    assert C % NV_BLOCK == 0
+    s_enc, s_dec = nvfp4_global(tensor_amax)
+    if block2d:
+        assert R % NV_BLOCK == 0
+        t = np.abs(z).reshape(R // 16, 16, C // 16, 16)
+        a_b = np.repeat(t.max(axis=(1, 3)), 16, axis=0)          # [R, C/16]
+    else:
+        a_b = np.max(np.abs(z.reshape(R, C // 16, 16)), axis=2)   # [R, C/16]
+    a_b = a_b.astype(np.float32)
+    pre = ((a_b / f32(6.0)).astype(np.float32) * s_enc).astype(np.float32)
+    s_codes = F.encode_ue4m3(pre)
+    s_val = F.decode_ue4m3(s_codes).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        r = np.where(s_val > 0, (s_enc / np.where(s_val > 0, s_val, f32(1.0))).astype(np.float32), f32(0.0))
+    r = r.astype(np.float32)
+    v = (z.reshape(R, C // 16, 16) * r[:, :, None]).astype(np.float32).reshape(R, C)
+    if sr is None:
+        q = F.encode(v, "e2m1")
+    else:
+        words = element_words(R * C, sr["row0"] * sr["cols"], sr["seed"], sr["copy_id"], sr["offset"])
+        q = e2m1_round_stochastic(v, words.reshape(R, C))
+    return q, s_codes, s_dec
+
+
+def pack_e2m1(codes) -> np.ndarray:
+    """Two nibbles per byte: element 2i in the low nibble, 2i+1 in the high nibble."""
+    c = np.asarray(codes).astype(np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    p = np.asarray(packed).astype(np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def nvfp4_dequant(codes, scales, s_dec) -> np.ndarray:
+    c = np.asarray(codes)
+    R, C = c.shape
+    val = F.decode(c, "e2m1").reshape(R, C // 16, 16)
+    sv = F.decode_ue4m3(scales)
+    return (val * sv[:, :, None] * float(s_dec)).reshape(R, C)

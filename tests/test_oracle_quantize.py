@@ -1,0 +1,244 @@
+"""Pins for oracle.quantize: closed forms, special cases, an explicit Hadamard
+matrix, statistics of stochastic rounding, and transpose consistency."""
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import quantize as Q
+
+rng = np.random.default_rng(42)
+
+
+def test_amax_exact_and_order_free():
+    x = rng.standard_normal((37, 53)).astype(np.float32)
+    x[5, 7] = -9.25
+    assert Q.amax(x) == np.float32(9.25)
+    assert Q.amax(x[::-1, ::-1]) == Q.amax(x)
+    assert Q.amax(np.array([-0.0, 0.0], np.float32)) == 0.0
+    assert Q.amax(np.zeros((0, 4), np.float32)) == 0.0
+    assert float(Q.amax(x)) == max(abs(float(v)) for v in x.ravel())
+
+
+def test_fp8_row_col_copies_are_transposes():
+    x = rng.standard_normal((64, 48)).astype(np.float32)
+    q_row, q_col, a, si = Q.fp8_quantize(x, np.float32(30.0), "e5m2")
+    np.testing.assert_array_equal(q_col, q_row.T)
+    assert si == np.float32(1) / np.float32(30)
+    # dequantization error bounded by half an E5M2 ulp (relative 2**-3) for normal values
+    deq = Q.fp8_dequant(q_row, si, "e5m2")
+    big = np.abs(x) > 2.0 ** -10
+    assert np.all(np.abs(deq[big] - x[big]) <= np.abs(x[big]) * 2.0 ** -3 + 1e-12)
+
+
+# ---- MXFP8 ----------------------------------------------------------------------
+
+def test_mx_power_of_two_block():
+    for k in (-20, 0, 3, 100):
+        z = np.full((1, 32), 2.0 ** k, np.float32)
+        q, s = Q.mxfp8_quantize(z)
+        assert int(s[0, 0]) == k - 8 + 127
+        assert np.all(q == 0x78)            # 2**8 in E4M3
+
+
+def test_mx_spike_hits_448_and_saturation():
+    z = np.zeros((1, 32), np.float32)
+    z[0, 3] = 1.75 * 2.0 ** 5
+    z[0, 9] = -1.0
+    q, s = Q.mxfp8_quantize(z)
+    assert int(s[0, 0]) == 5 - 8 + 127
+    assert q[0, 3] == 0x7E
+    z[0, 3] = 1.99 * 2.0 ** 5                # 1.99 * 2**8 after scaling -> saturates to 448
+    q, _ = Q.mxfp8_quantize(z)
+    assert q[0, 3] == 0x7E
+
+
+def test_mx_zero_block_and_clamp():
+    q, s = Q.mxfp8_quantize(np.zeros((2, 64), np.float32))
+    assert np.all(s == 0) and np.all(q == 0)
+    tiny = np.full((1, 32), 2.0 ** -140, np.float32)   # floor(log2) - 8 = -148 -> clamp -127
+    q, s = Q.mxfp8_quantize(tiny)
+    assert int(s[0, 0]) == 0
+    # x * 2**127 = 2**-13 is below E4M3's smallest subnormal (2**-9): quantizes to zero
+    assert np.all(q == 0)
+
+
+def test_mx_dequant_reproduces_representable_values():
+    # blocks whose elements are E4M3 values times 2**E, with the block max in [256, 448]
+    R, C = 8, 64
+    codes = rng.integers(0, 0x7F, size=(R, C))
+    codes[:, ::32] = rng.integers(0x78, 0x7F, size=(R, C // 32))   # exponent field 15 -> [256, 448]
+    signs = rng.integers(0, 2, size=(R, C)) << 7
+    E = rng.integers(-100, 100, size=(R, C // 32))
+    vals = F.decode(codes | signs, "e4m3") * np.exp2(np.repeat(E, 32, axis=1))
+    z = vals.astype(np.float32)
+    assert np.all(z.astype(np.float64) == vals)
+    q, s = Q.mxfp8_quantize(z)
+    np.testing.assert_array_equal(s.astype(np.int64) - 127, E)
+    np.testing.assert_array_equal(Q.mxfp8_dequant(q, s), vals)
+
+
+# ---- RHT ---------------------------------------------------------------------------
+
+def _hadamard16():
+    i = np.arange(16)
+    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+def test_rht_matches_explicit_matrix():
+    signs = 0b1010_0110_0011_1001
+    H = _hadamard16()
+    D = np.diag([-1.0 if (signs >> j) & 1 else 1.0 for j in range(16)])
+    z = rng.standard_normal((5, 64)).astype(np.float32)
+    y = Q.rht16(z, signs)
+    ref = (z.astype(np.float64).reshape(-1, 16) @ (0.25 * H @ D).T).reshape(5, 64)
+    # four fp32 rounding stages of sums of up to 16 terms
+    assert np.max(np.abs(y - ref)) <= 1e-5 * np.max(np.abs(ref))
+    # small integers: every butterfly is exact, so the result is exact
+    zi = rng.integers(-50, 50, size=(3, 32)).astype(np.float32)
+    yi = Q.rht16(zi, signs)
+    refi = (zi.astype(np.float64).reshape(-1, 16) @ (0.25 * H @ D).T).reshape(3, 32)
+    np.testing.assert_array_equal(yi, refi)
+
+
+def test_rht_one_hot_inverse_and_dot_products():
+    for j in range(16):
+        e = np.zeros((1, 16), np.float32)
+        e[0, j] = 1.0
+        y = Q.rht16(e, 0)
+        assert np.all(np.abs(y) == 0.25)
+    signs = 0x5A3C
+    x = rng.standard_normal((4, 48)).astype(np.float32)
+    y = Q.rht16(x, signs)
+    back = Q.rht16(y, 0) * 4.0                       # 1/4 H (1/4 H D x) * 4 = D x / ... = D x
+    dvec = np.array([-1.0 if (signs >> j) & 1 else 1.0 for j in range(16)], np.float32)
+    rec = (back.reshape(-1, 16) * dvec).reshape(x.shape) / 4.0
+    np.testing.assert_allclose(rec, x, rtol=0, atol=1e-6 * np.abs(x).max())
+    a = rng.standard_normal((1, 4096)).astype(np.float32)
+    b = rng.standard_normal((1, 4096)).astype(np.float32)
+    lhs = np.dot(Q.rht16(a, signs)[0].astype(np.float64), Q.rht16(b, signs)[0].astype(np.float64))
+    rhs = np.dot(a[0].astype(np.float64), b[0].astype(np.float64))
+    assert abs(lhs - rhs) <= 1e-4 * np.sqrt(4096)
+
+
+# ---- NVFP4 ----------------------------------------------------------------------------
+
+def test_nvfp4_global_scales():
+    s, d = Q.nvfp4_global(np.float32(2688.0))
+    assert s == 1.0 and d == 1.0
+    s, d = Q.nvfp4_global(np.float32(0.0))
+    assert s == 1.0 and d == 1.0
+    s, d = Q.nvfp4_global(np.float32(1e-45))
+    assert s == 1.0
+    s, d = Q.nvfp4_global(np.float32(6.0))
+    assert s == 448.0 and d == np.float32(1) / np.float32(448)
+
+
+def test_nvfp4_block_at_tensor_amax_scales_to_448_and_6():
+    z = rng.standard_normal((4, 64)).astype(np.float32)
+    A = Q.amax(z)
+    q, s, sd = Q.nvfp4_quantize(z, A)
+    r, c = np.unravel_index(np.argmax(np.abs(z)), z.shape)
+    assert s[r, c // 16] == 0x7E                  # 448
+    assert q[r, c] & 0x7 == 0x7                   # |6|
+    assert (q[r, c] >> 3) == (1 if z[r, c] < 0 else 0)
+
+
+def test_nvfp4_uniform_block_all_six():
+    for c in (0.3, 1.0, 7.7, 123.0):
+        z = np.full((1, 16), c, np.float32)
+        z = np.concatenate([z, np.full((1, 16), 1000.0, np.float32)], axis=1)  # tensor amax elsewhere
+        q, s, _ = Q.nvfp4_quantize(z, Q.amax(z))
+        assert F.decode_ue4m3(s[:, :1])[0, 0] >= 2.0 ** -6        # normal UE4M3
+        assert np.all(q[0, :16] == 0x7)
+
+
+def test_nvfp4_zero_tensor_and_zero_scale_block():
+    q, s, sd = Q.nvfp4_quantize(np.zeros((2, 32), np.float32), 0.0)
+    assert np.all(q == 0) and np.all(s == 0) and sd == 1.0
+    z = np.zeros((1, 32), np.float32)
+    z[0, 0] = 1.0
+    z[0, 20] = -1e-9                               # block scale rounds to 0 -> r = 0 -> signed zero
+    q, s, _ = Q.nvfp4_quantize(z, Q.amax(z))
+    assert s[0, 1] == 0 and q[0, 20] == 0x8 and q[0, 21] == 0x0
+
+
+def test_nvfp4_2d_transpose_consistency():
+    w = (rng.standard_normal((48, 64)) * 0.02).astype(np.float32)
+    A = Q.amax(w)
+    q_r, s_r, _ = Q.nvfp4_quantize(w, A, block2d=True)
+    q_c, s_c, _ = Q.nvfp4_quantize(np.ascontiguousarray(w.T), A, block2d=True)
+    np.testing.assert_array_equal(q_c, q_r.T)
+    # each 16x16 tile has one scale, replicated along both copies
+    tile_r = s_r.reshape(3, 16, 4)
+    assert np.all(tile_r == tile_r[:, :1, :])
+    np.testing.assert_array_equal(s_c.reshape(4, 16, 3)[:, 0, :], tile_r[:, 0, :].T)
+
+
+def test_nvfp4_dequant_error_bound():
+    z = rng.standard_normal((32, 256)).astype(np.float32)
+    A = Q.amax(z)
+    q, s, sd = Q.nvfp4_quantize(z, A)
+    deq = Q.nvfp4_dequant(q, s, sd)
+    # element error <= half the E2M1 spacing at the block's scale (spacing <= 2 * unit), plus scale rounding
+    unit = F.decode_ue4m3(s) * float(sd)
+    bound = np.repeat(unit, 16, axis=1) * 1.0 + 1e-12
+    assert np.all(np.abs(deq - z) <= bound)
+    assert Q.amax(deq) <= A * (1 + 2.0 ** -3)
+
+
+def test_pack_unpack_nibble_order():
+    c = np.array([[1, 2, 3, 15, 0, 8]], np.uint8)
+    p = Q.pack_e2m1(c)
+    assert list(p[0]) == [0x21, 0xF3, 0x80]
+    np.testing.assert_array_equal(Q.unpack_e2m1(p), c)
+
+
+# ---- stochastic rounding ----------------------------------------------------------------
+
+def test_sr_exact_values_never_move_and_neighbours_only():
+    grid = np.concatenate([Q.E2M1_GRID, -Q.E2M1_GRID]).astype(np.float32)
+    words = rng.integers(0, 1 << 32, size=grid.size, dtype=np.uint64).astype(np.uint32)
+    np.testing.assert_array_equal(Q.e2m1_round_stochastic(grid, words), F.encode(grid, "e2m1"))
+    v = rng.uniform(-7, 7, size=4096).astype(np.float32)
+    words = rng.integers(0, 1 << 32, size=v.size, dtype=np.uint64).astype(np.uint32)
+    got = F.decode(Q.e2m1_round_stochastic(v, words), "e2m1")
+    a = np.minimum(np.abs(v), 6.0)
+    lo = Q.E2M1_GRID[np.clip(np.searchsorted(Q.E2M1_GRID, a, side="right") - 1, 0, 7)]
+    hi = Q.E2M1_GRID[np.clip(np.searchsorted(Q.E2M1_GRID, a, side="left"), 0, 7)]
+    assert np.all((np.abs(got) == lo) | (np.abs(got) == hi))
+    assert np.all(np.sign(got)[got != 0] == np.sign(v)[got != 0])
+
+
+def test_sr_threshold_rule():
+    # frac = 0.25 at v = 2.25 (between 2 and 3): up iff (w >> 8) < 0.25 * 2**24
+    v = np.full(4, 2.25, np.float32)
+    w = np.array([0, (1 << 22) - 1, 1 << 22, 0xFFFFFFFF], np.uint64) << np.uint64(8)
+    w = (w & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    got = F.decode(Q.e2m1_round_stochastic(v, w), "e2m1")
+    assert list(got) == [3.0, 3.0, 2.0, 2.0]
+
+
+@pytest.mark.parametrize("v", [0.1, 0.8, 1.3, 2.6, 3.3, 4.9, 5.99])
+def test_sr_unbiased(v):
+    n = 1 << 18
+    from oracle.philox import element_words
+    words = element_words(n, 0, seed=977, copy_id=0, offset=int(v * 100))
+    got = F.decode(Q.e2m1_round_stochastic(np.full(n, v, np.float32), words), "e2m1")
+    lo = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v) - 1]
+    hi = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v)]
+    p = (v - lo) / (hi - lo)
+    sigma = (hi - lo) * np.sqrt(p * (1 - p) / n)
+    assert abs(got.mean() - np.float32(v)) < 4 * sigma + 1e-7
+
+
+def test_nvfp4_sr_uses_copy_indexed_words():
+    z = rng.standard_normal((32, 64)).astype(np.float32)
+    A = Q.amax(z)
+    sr = dict(seed=11, copy_id=1, offset=5, row0=0, cols=64)
+    q_full, _, _ = Q.nvfp4_quantize(z, A, sr=sr)
+    sr2 = dict(sr, row0=8)
+    q_part, _, _ = Q.nvfp4_quantize(z[8:16], A, sr=sr2)
+    np.testing.assert_array_equal(q_full[8:16], q_part)
+    q_rn, _, _ = Q.nvfp4_quantize(z, A)
+    assert np.mean(q_rn != q_full) > 0.05       # SR really differs from RN on random data
