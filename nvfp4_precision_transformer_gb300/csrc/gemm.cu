@@ -1,0 +1,451 @@
+// Tensor-core GEMMs for sm_103a: D = alpha * A B^T (+ bias), A [M, K] and B [N, K]
+// contraction-major, fp32 accumulation in tensor memory (TMEM).
+//
+// One persistent kernel template serves the four operand kinds:
+//   BF16   tcgen05.mma kind::f16              K = 16 per instruction
+//   FP8    tcgen05.mma kind::f8f6f4           K = 32, per-tensor alpha in the epilogue
+//   MXFP8  tcgen05.mma kind::mxf8f6f4         K = 32, E8M0 scale per 32 elements (block_scale 1X)
+//   NVFP4  tcgen05.mma kind::mxf4nvf4         K = 64, UE4M3 scale per 16 elements (block_scale 4X)
+// Every kind moves 32 bytes of each operand row per instruction, so one k-tile
+// is a 128-byte row slice (one 128-byte-swizzle atom) and 4 instructions.
+//
+// CTA = 10 warps, one CTA per SM (the shared-memory footprint guarantees it):
+//   warp 0      TMA producer: A tile [128 x 128 B], B tile [256 x 128 B] and, for the
+//               block-scaled kinds, the scale-factor atoms (bulk copies), into a
+//               4-stage shared-memory ring guarded by full/empty mbarriers;
+//   warp 1      allocates TMEM and issues the MMAs from one thread: scale factors
+//               are copied smem -> TMEM with tcgen05.cp, each k-tile's MMAs are
+//               followed by tcgen05.commit onto the stage's empty barrier, each
+//               tile's last k-tile by a commit onto the accumulator-full barrier;
+//   warps 2-9   epilogue: each warp owns a 32-lane quarter of TMEM and a 128-column
+//               half of the 128 x 256 accumulator, drains it to registers, releases
+//               the accumulator, then applies alpha / bias, rounds and stores.
+// The accumulator is double-buffered in TMEM for BF16/FP8 (2 x 256 columns); the
+// block-scaled kinds keep one 256-column accumulator plus a per-stage scale-factor
+// region and rely on the early release of the register drain for overlap.
+// Tiles are visited in a grouped raster (8 M-tiles per group) so concurrently
+// running CTAs share A and B tiles in L2.  No cluster multicast is used.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace te {
+namespace {
+
+enum Kind { kBF16 = 0, kFP8 = 1, kMXFP8 = 2, kNVFP4 = 3 };
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kGroupM = 8;
+constexpr uint32_t kTmemCols = 512;
+
+template <int KIND>
+struct Cfg {
+  static constexpr bool kBlockScaled = KIND >= kMXFP8;
+  static constexpr int kAccStages = kBlockScaled ? 1 : 2;
+  static constexpr int kABytes = BM * 128;
+  static constexpr int kBBytes = BN * 128;
+  // scale-factor atoms (512 B = 128 rows x 4 scales) per 128 rows per k-tile
+  static constexpr int kSfAtoms = KIND == kMXFP8 ? 1 : (KIND == kNVFP4 ? 4 : 0);
+  static constexpr int kSfaBytes = kSfAtoms * 512;
+  static constexpr int kSfbBytes = 2 * kSfAtoms * 512;
+  static constexpr int kSfaCols = 4 * kSfAtoms;
+  static constexpr int kSfbCols = 8 * kSfAtoms;
+  static constexpr int kSfTmemBase = 256;
+  static constexpr int kSmemA = 0;
+  static constexpr int kSmemB = kSmemA + kStages * kABytes;
+  static constexpr int kSmemSfa = kSmemB + kStages * kBBytes;
+  static constexpr int kSmemSfb = kSmemSfa + kStages * kSfaBytes;
+  static constexpr int kSmemBar = kSmemSfb + kStages * kSfbBytes;
+  static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
+  static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int k_tiles, m_tiles, n_tiles;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int64_t sf_katoms;    // scale atoms per 128-row group (padded scale columns / 4)
+  int sfb_row_atoms;    // 128-row groups present in B's scale tensor
+  const float* alpha_a;
+  const float* alpha_b;
+  const float* bias;
+  void* D;
+  int out_f32;
+  uint32_t idesc;
+  int* err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int group = kGroupM * n_tiles;
+  const int g = tile / group;
+  const int first_m = g * kGroupM;
+  const int gm = min(m_tiles - first_m, kGroupM);
+  const int in_group = tile - g * group;
+  mt = first_m + in_group % gm;
+  nt = in_group / gm;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmArgs args) {
+  using C = Cfg<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = dev::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem + C::kSmemA;
+  uint8_t* sB = smem + C::kSmemB;
+  uint8_t* sSfa = smem + C::kSmemSfa;
+  uint8_t* sSfb = smem + C::kSmemSfb;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kSmemBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = args.m_tiles * args.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      dev::mbar_init(&acc_full[s], 1);
+      dev::mbar_init(&acc_empty[s], kEpiWarps);
+    }
+    dev::mbar_init(drain, 1);
+    *abort_flag = 0;
+    dev::fence_barrier_init();
+    dev::prefetch_tmap(&tmA);
+    dev::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) dev::tmem_alloc(tmem_slot, kTmemCols);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[kStages];
+      bool issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
+      const uint32_t tx = C::kABytes + C::kBBytes + C::kSfaBytes;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
+        for (int kt = 0; kt < args.k_tiles; ++kt) {
+          if (!dev::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          uint32_t bytes = tx;
+          int sfb_halves = 0;
+          if (C::kBlockScaled) {
+            for (int h = 0; h < 2; ++h)
+              if (nt * 2 + h < args.sfb_row_atoms) ++sfb_halves;
+            bytes += sfb_halves * C::kSfAtoms * 512;
+          }
+          dev::mbar_expect_tx(&full[stage], bytes);
+          dev::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, mt * BM);
+          dev::tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, nt * BN);
+          if (C::kBlockScaled) {
+            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
+            dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
+                           C::kSfaBytes, &full[stage]);
+            for (int h = 0; h < 2; ++h) {
+              const int ra = nt * 2 + h;
+              if (ra < args.sfb_row_atoms)
+                dev::bulk_load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512,
+                               args.sfb + (ra * args.sf_katoms + katom) * 512, C::kSfAtoms * 512, &full[stage]);
+            }
+          }
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // Bounded wait for our own copies still in flight before the CTA exits.
+        volatile int dummy = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) dev::mbar_wait(&full[s], issued_phase[s], &dummy, args.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+        const int as = it % C::kAccStages;
+        const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
+        if (!dev::mbar_wait(&acc_empty[as], aphase ^ 1u, abort_flag, args.err)) {
+          ok = false;
+          break;
+        }
+        dev::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
+        for (int kt = 0; kt < args.k_tiles; ++kt) {
+          if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          dev::tc_fence_after();
+          const uint32_t a_addr = dev::smem_u32(sA + stage * C::kABytes);
+          const uint32_t b_addr = dev::smem_u32(sB + stage * C::kBBytes);
+          uint32_t sfa_t = 0, sfb_t = 0;
+          if (C::kBlockScaled) {
+            sfa_t = tmem_base + C::kSfTmemBase + stage * (C::kSfaCols + C::kSfbCols);
+            sfb_t = sfa_t + C::kSfaCols;
+            const uint32_t sfa_s = dev::smem_u32(sSfa + stage * C::kSfaBytes);
+            const uint32_t sfb_s = dev::smem_u32(sSfb + stage * C::kSfbBytes);
+#pragma unroll
+            for (int j = 0; j < C::kSfAtoms; ++j) {
+              dev::tc_cp_32x128b_x4(sfa_t + 4 * j, dev::smem_desc(sfa_s + 512 * j, 0, 128, 0));
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                dev::tc_cp_32x128b_x4(sfb_t + 8 * j + 4 * h,
+                                      dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
+            }
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t adesc = dev::smem_desc(a_addr + 32 * ks, 0, 1024, 2);
+            const uint64_t bdesc = dev::smem_desc(b_addr + 32 * ks, 0, 1024, 2);
+            const uint32_t acc = (kt | ks) != 0;
+            if (KIND == kBF16) {
+              dev::mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
+            } else if (KIND == kFP8) {
+              dev::mma_f8f6f4(d_tmem, adesc, bdesc, args.idesc, acc);
+            } else if (KIND == kMXFP8) {
+              // scale byte `ks` of each 32-bit scale column (bits 29-30: A, bits 4-5: B)
+              const uint32_t idesc = args.idesc | (static_cast<uint32_t>(ks) << 29) | (static_cast<uint32_t>(ks) << 4);
+              dev::mma_mxf8f6f4(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, acc);
+            } else {
+              dev::mma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_t + 8 * ks, acc);
+            }
+          }
+          dev::tc_commit(&empty[stage]);
+          if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        dev::tc_commit(&acc_full[as]);
+      }
+      // Every tcgen05 operation issued above completes before this commit fires.
+      dev::tc_commit(drain);
+      volatile int dummy = 0;
+      dev::mbar_wait(drain, 0, &dummy, args.err);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const float alpha = (args.alpha_a ? __ldg(args.alpha_a) : 1.0f) * (args.alpha_b ? __ldg(args.alpha_b) : 1.0f);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      int mt, nt;
+      tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
+      const int as = it % C::kAccStages;
+      const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
+      if (!dev::mbar_wait(&acc_full[as], aphase, abort_flag, args.err)) break;
+      dev::tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(as * BN + half * 128);
+      uint32_t acc[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) dev::tmem_ld_32x32b_x32(taddr + 32 * c, acc[c]);
+      dev::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) dev::reg_fence(acc[c]);
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&acc_empty[as]);
+
+      const int m = mt * BM + quarter * 32 + lane;
+      const int n0 = nt * BN + half * 128;
+      if (m < args.M) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // 8 columns = 16 bytes of bf16 / 32 bytes of fp32
+            const int n = n0 + 32 * c + 8 * q;
+            if (n >= args.N) continue;
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float b = args.bias ? __ldg(args.bias + n + i) : 0.0f;
+              v[i] = __fmaf_rn(__uint_as_float(acc[c][8 * q + i]), alpha, b);
+            }
+            if (args.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.D) + static_cast<int64_t>(m) * args.N + n);
+              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+            } else {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.D) + static_cast<int64_t>(m) * args.N + n) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  if (warp == 1) dev::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---- host launch ----------------------------------------------------------------------------------
+
+// Instruction descriptor (tcgen05, dense): D format in bits 4-5 (F32 = 1) for the
+// non-block-scaled kinds, A / B formats in bits 7-9 / 10-12, K-major operands
+// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28; for the
+// block-scaled kinds bit 23 selects the scale format (UE8M0 = 1, UE4M3 = 0).
+uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt) {
+  uint32_t d = 0;
+  if (kind == kBF16 || kind == kFP8) d |= 1u << 4;
+  d |= (afmt & 7u) << 7;
+  d |= (bfmt & 7u) << 10;
+  d |= static_cast<uint32_t>(BN >> 3) << 17;
+  if (kind == kMXFP8) d |= 1u << 23;
+  d |= static_cast<uint32_t>(BM >> 4) << 24;
+  return d;
+}
+
+template <int KIND>
+te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
+                      int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
+                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st) {
+  using C = Cfg<KIND>;
+  static bool attr_set[64] = {false};
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
+    if (cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTotal) !=
+        cudaSuccess)
+      return record_cuda(cudaGetLastError());
+    attr_set[dev_id] = true;
+  }
+  CUtensorMap ta, tb;
+  te_status s = make_tmap_2d(&ta, A, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(M), BM);
+  if (s != TE_OK) return s;
+  s = make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
+  if (s != TE_OK) return s;
+  int* err = device_error_word();
+  if (err == nullptr) return record_cuda(cudaErrorInvalidDevice);
+  GemmArgs g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.k_tiles = static_cast<int>((row_bytes + 127) / 128);
+  g.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  g.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  g.sfa = sfa;
+  g.sfb = sfb;
+  g.sf_katoms = sf_katoms;
+  g.sfb_row_atoms = static_cast<int>((N + 127) / 128);
+  g.alpha_a = alpha_a;
+  g.alpha_b = alpha_b;
+  g.bias = bias;
+  g.D = D;
+  g.out_f32 = out == TE_F32;
+  g.idesc = make_idesc(KIND, afmt, bfmt);
+  g.err = err;
+  const int tiles = g.m_tiles * g.n_tiles;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_kernel<KIND><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, g);
+  count_launch();
+  return launch_status();
+}
+
+te_status check_gemm(const void* A, const void* B, const void* D, te_dtype out, int64_t M, int64_t N, int64_t K,
+                     int64_t k_multiple) {
+  if (out != TE_BF16 && out != TE_F32) return TE_ERR_DTYPE;
+  if (M < 0 || N < 0 || K <= 0 || M % 16 || N % 16 || K % k_multiple) return TE_ERR_SHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return TE_ERR_SHAPE;
+  if (M * N == 0) return TE_OK;
+  if (!A || !B || !D) return TE_ERR_NULL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return TE_ERR_ALIGN;
+  return TE_OK;
+}
+
+inline bool fp8_fmt(te_dtype f) { return f == TE_E4M3 || f == TE_E5M2; }
+inline uint32_t f8_code(te_dtype f) { return f == TE_E5M2 ? 1u : 0u; }
+
+}  // namespace
+}  // namespace te
+
+using namespace te;
+
+extern "C" {
+
+te_status te_gemm_bf16(const void* A, const void* B, const float* bias, void* D, te_dtype out_dtype, int64_t M,
+                       int64_t N, int64_t K, void* stream) {
+  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
+  if (s != TE_OK || M * N == 0) return s;
+  return launch_gemm<kBF16>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, M, N, K, 1u, 1u,
+                            static_cast<cudaStream_t>(stream));
+}
+
+te_status te_gemm_fp8(const uint8_t* A, te_dtype fa, const uint8_t* B, te_dtype fb, const float* a_scale_inv,
+                      const float* b_scale_inv, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
+                      int64_t K, void* stream) {
+  if (!fp8_fmt(fa) || !fp8_fmt(fb)) return TE_ERR_DTYPE;
+  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
+  if (s != TE_OK || M * N == 0) return s;
+  if (!a_scale_inv || !b_scale_inv) return TE_ERR_NULL;
+  return launch_gemm<kFP8>(A, B, K, nullptr, nullptr, 0, a_scale_inv, b_scale_inv, bias, D, out_dtype, M, N, K,
+                           f8_code(fa), f8_code(fb), static_cast<cudaStream_t>(stream));
+}
+
+te_status te_gemm_mxfp8(const uint8_t* A, te_dtype fa, const uint8_t* sA, const uint8_t* B, te_dtype fb,
+                        const uint8_t* sB, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
+                        int64_t K, void* stream) {
+  if (!fp8_fmt(fa) || !fp8_fmt(fb)) return TE_ERR_DTYPE;
+  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 32);
+  if (s != TE_OK || M * N == 0) return s;
+  if (!sA || !sB) return TE_ERR_NULL;
+  if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
+  const int64_t katoms = ((K / 32 + 3) / 4);
+  return launch_gemm<kMXFP8>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
+                             f8_code(fb), static_cast<cudaStream_t>(stream));
+}
+
+te_status te_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA, const uint8_t* B, const uint8_t* sB,
+                        const float* gB, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
+                        int64_t K, void* stream) {
+  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 32);
+  if (s != TE_OK || M * N == 0) return s;
+  if (!sA || !sB || !gA || !gB) return TE_ERR_NULL;
+  if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
+  const int64_t katoms = ((K / 16 + 15) / 16) * 4;
+  return launch_gemm<kNVFP4>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
+                             static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
