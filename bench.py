@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Per-layer GEMM benchmark of the quantized linear-layer hot path on GB300.
+
+Workload: one CodonFM-5B-shaped transformer layer (hidden 4096, intermediate
+16384, micro-batch 31 x sequence 512 = 15872 tokens): four linears x Fprop /
+Dgrad / Wgrad = 12 GEMMs, 19.17 TFLOP ("How to Optimize Transformer-Based
+Models for Low-Precision Training", sections "モデル設定とトレーニング入力" and
+"autocast モードの使用と事前量子化の比較").  Inputs are synthetic and seeded
+(X ~ N(0,1), W ~ N(0,0.02^2), dY ~ N(0,1e-3^2), bf16); no dataset, no weights.
+
+One timed step runs, for each recipe (bf16, fp8_delayed, fp8_current, mxfp8,
+nvfp4), the layer in autocast mode (both operands quantized before every GEMM)
+and then in pre-quantized mode (the 12 GEMMs alone on the operands the
+autocast pass produced).  The headline ``value`` is the FP8 CurrentScaling
+autocast time per layer; every recipe and mode is in ``per_recipe``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the layer (the path
+has no exchange step on one node's replicas), the timed region is bracketed by
+a barrier and the maximum over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ms and TFLOP/s per layer GEMMs (autocast & pre-quantized), % of tensor/HBM peak"
+# The pages' per-layer numbers (B300 SXM6 AC, autocast unless noted): context, not targets.
+PAGES_MS = {("fp8_delayed", "autocast"): 7.80, ("fp8_current", "autocast"): 9.15, ("mxfp8", "autocast"): 8.98,
+            ("fp8_current", "prequant"): 6.81}
+HEADLINE = ("fp8_current", "autocast")
+RECIPE_DTYPE = {"bf16": "bf16", "fp8_delayed": "fp8", "fp8_current": "fp8", "mxfp8": "fp8", "nvfp4": "fp4"}
+PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}   # nominal dense ratios to bf16 (2.25 / 4.5 / 13.5 PF)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--recipes", default="bf16,fp8_delayed,fp8_current,mxfp8,nvfp4")
+    p.add_argument("--tokens", type=int, default=31 * 512)
+    p.add_argument("--hidden", type=int, default=4096)
+    p.add_argument("--ffn", type=int, default=16384)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    return p.parse_args()
+
+
+# ---- distributed plumbing (replicas) -------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int) -> float:
+    """Maximum of a host float over ranks (identity for a single process)."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- clocks -----------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_index)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- measured peaks ------------------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---- CPU oracle baseline ---------------------------------------------------------------------------
+
+def oracle_sample(tokens_sample: int, hidden: int, cfg_tokens: int, layer_flops: float, layer_elems: float):
+    """Time the oracle (as it stands) on FP8 CurrentScaling autocast Fprop of the attention-output
+    linear restricted to ``tokens_sample`` tokens: amax of X and W, FP8 quantization of the X slab
+    and of W, fp64 GEMM + bias.  Returns (ms per layer extrapolated, description, seconds)."""
+    import numpy as np
+    from oracle import gemm as OG, quantize as Q, recipes as Rc
+    from oracle.formats import bf16_bits_to_f32
+    from synthetic import gaussian, bf16_bits
+    x = bf16_bits_to_f32(bf16_bits(gaussian((tokens_sample, hidden), 1.0, 901)))
+    w = bf16_bits_to_f32(bf16_bits(gaussian((hidden, hidden), 0.02, 902)))
+    b = np.zeros(hidden, np.float32)
+    t0 = time.perf_counter()
+    sx, ix = Rc.current_scale(Q.amax(x), "e4m3")
+    sw, iw = Rc.current_scale(Q.amax(w), "e4m3")
+    qx = Q.fp8_cast(x, sx, "e4m3")
+    qw = Q.fp8_cast(w, sw, "e4m3")
+    t1 = time.perf_counter()
+    OG.gemm(Q.fp8_dequant(qx, ix, "e4m3"), Q.fp8_dequant(qw, iw, "e4m3"), bias=b)
+    t2 = time.perf_counter()
+    q_per_elem = (t1 - t0) / (x.size + w.size)
+    g_per_flop = (t2 - t1) / (2.0 * tokens_sample * hidden * hidden)
+    ms = 1e3 * (q_per_elem * layer_elems + g_per_flop * layer_flops)
+    desc = (f"oracle FP8-current Fprop of attn_out on {tokens_sample} tokens x {hidden} (+ W {hidden}x{hidden}); "
+            f"extrapolated per element quantized ({layer_elems:.3g}/layer) and per GEMM flop ({layer_flops:.3g}/layer)")
+    return ms, desc, t2 - t0
+
+
+def cpu_threads():
+    return os.cpu_count() or 1
+
+
+# ---- reference arm -------------------------------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from nvfp4_precision_transformer_gb300.shapes import LayerConfig, layer_flops, linears
+    cfg = LayerConfig(hidden=args.hidden, intermediate=args.ffn, micro_batch=1, seq_len=args.tokens)
+    lf = float(layer_flops(cfg))
+    elems = 2.0 * sum(cfg.tokens * ki + no * ki + cfg.tokens * no for _, ki, no in linears(cfg))
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        ms, desc, _ = oracle_sample(64, args.hidden, cfg.tokens, lf, elems)
+        if i >= args.warmup:
+            times.append(ms)
+    v = statistics.median(times)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "ms/layer", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args),
+            "cpu_baseline": {"value": v, "unit": "ms/layer", "cores": cpu_threads(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args):
+    return {"workload": f"CodonFM-5B layer GEMMs: M={args.tokens} tokens, hidden {args.hidden}, ffn {args.ffn}, "
+                        f"12 shapes (QKV/attn-out/MLP-up/MLP-down x Fprop/Dgrad/Wgrad); headline FP8 "
+                        f"CurrentScaling HYBRID (E4M3 X/W, E5M2 dY), autocast",
+            "tokens": args.tokens, "hidden": args.hidden, "ffn": args.ffn, "recipe": "fp8_current",
+            "l2": "inputs larger than L2 (X, W, dY of the layer: ~2.5 GB bf16 per step)",
+            "parallelism": "replicas"}
+
+
+# ---- our arm ---------------------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import nvfp4_precision_transformer_gb300 as te
+    from nvfp4_precision_transformer_gb300.linear import Layer
+    from nvfp4_precision_transformer_gb300.shapes import LayerConfig, layer_flops, linears
+    from synthetic import gaussian, rht_sign_mask, seed_for
+
+    assert torch.cuda.is_available(), "bench.py needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    recipes = [r for r in args.recipes.split(",") if r]
+    cfg = LayerConfig(hidden=args.hidden, intermediate=args.ffn, micro_batch=1, seq_len=args.tokens)
+    lf = float(layer_flops(cfg))
+
+    tensors = []
+    for i, (_, k_in, n_out) in enumerate(linears(cfg)):
+        x = gaussian((cfg.tokens, k_in), 1.0, seed_for(2, i, 0) + 97 * rank, device=dev)
+        w = gaussian((n_out, k_in), 0.02, seed_for(2, i, 1), device=dev)
+        dy = gaussian((cfg.tokens, n_out), 1e-3, seed_for(2, i, 2) + 97 * rank, device=dev)
+        b = gaussian((n_out,), 0.02, seed_for(2, i, 3), dtype=torch.float32, device=dev)
+        tensors.append((x, w, dy, b))
+    layer = Layer(tensors, recipes, history_len=16, rht_signs=rht_sign_mask(7), sr_seed=1234, device=dev)
+
+    modes = []
+    for r in recipes:
+        modes.append((r, "autocast"))
+        if r != "bf16":
+            modes.append((r, "prequant"))
+
+    def one_step(rec):
+        for r, m in modes:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            gemms = []
+
+            def on_gemm(lin, p, phase, _g=gemms):
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record()
+                if phase == 0:
+                    _g.append([lin.gemm_shape(p), ev, None])
+                else:
+                    _g[-1][2] = ev
+            e0.record()
+            layer.run(r, autocast=(m == "autocast"), on_gemm=on_gemm if rec is not None else None)
+            e1.record()
+            if rec is not None:
+                rec.append((r, m, e0, e1, gemms))
+        layer.step_idx += 1
+
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    barrier(ws)
+
+    records = []
+    launches0 = te.te_launch_count()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(ws)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record()
+        for _ in range(args.steps):
+            one_step(records)
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+    launches = te.te_launch_count() - launches0
+    assert te.te_get_last_error() == 0, "device error during the timed region"
+    total_ms = reduce_max(t_start.elapsed_time(t_end), ws)
+    clocks = clk.summary()
+
+    # per recipe / mode aggregation
+    pk = peaks()
+    agg = {}
+    for r, m, e0, e1, gemms in records:
+        d = agg.setdefault((r, m), {"seg": [], "gemm_ms": 0.0, "gemm_flops": 0.0})
+        d["seg"].append(e0.elapsed_time(e1))
+        for (M, N, K), g0, g1 in gemms:
+            d["gemm_ms"] += g0.elapsed_time(g1)
+            d["gemm_flops"] += 2.0 * M * N * K
+    per = {}
+    for (r, m), d in agg.items():
+        ms = statistics.mean(d["seg"])
+        peak = pk["bf16_tflops_sustained"] * PEAK_RATIO[RECIPE_DTYPE[r]]
+        gemm_tflops = d["gemm_flops"] / (d["gemm_ms"] * 1e-3) / 1e12
+        per[f"{r}/{m}"] = {"ms_per_layer": round(ms, 4), "tflops": round(lf / (ms * 1e-3) / 1e12, 1),
+                           "frac_of_peak": round(lf / (ms * 1e-3) / 1e12 / peak, 4),
+                           "gemm_ms_per_layer": round(d["gemm_ms"] / args.steps, 4),
+                           "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_peak": round(gemm_tflops / peak, 4),
+                           "peak_tflops": round(peak, 1),
+                           "pages_ms_b300": PAGES_MS.get((r, m))}
+    head = per.get(f"{HEADLINE[0]}/{HEADLINE[1]}") or next(iter(per.values()))
+    head_ms = reduce_max(head["ms_per_layer"], ws) / ws          # whole job: ws replicas in parallel
+    # dominant kernel of the headline: the FP8 GEMM
+    hd = agg.get(HEADLINE) or next(iter(agg.values()))
+    fp8_peak = pk["bf16_tflops_sustained"] * PEAK_RATIO["fp8"]
+    achieved = hd["gemm_flops"] / (hd["gemm_ms"] * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_kernel<FP8> (tcgen05 kind::f8f6f4)", "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                "traffic": None,
+                "peak_note": f"{pk['source']} bf16 sustained {pk['bf16_tflops_sustained']} x 2 (nominal FP8/BF16 ratio)",
+                "launches_per_layer": 12}
+
+    line = {"metric": METRIC, "value": round(head_ms, 4), "unit": "ms/layer", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": round(head_ms / PAGES_MS[HEADLINE], 4), "dtype": "fp8",
+            "data": "synthetic", "config": workload_config(args), "per_recipe": per, "roofline": roofline,
+            "gpu_launches": int(launches), "clocks": clocks}
+
+    # end to end through the C ABI from pinned host buffers (headline recipe)
+    if not args.no_e2e and HEADLINE[0] in recipes:
+        line["e2e"] = run_e2e(layer, args, ws)
+    if rank == 0 and not args.no_cpu:
+        elems = 2.0 * sum(cfg.tokens * ki + no * ki + cfg.tokens * no for _, ki, no in linears(cfg))
+        ms, desc, secs = oracle_sample(256, args.hidden, cfg.tokens, lf, elems)
+        line["cpu_baseline"] = {"value": round(ms, 1), "unit": "ms/layer", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": desc, "sample_seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(layer, args, ws):
+    import torch
+    lins = layer.linears
+    host_in = [(l.x.cpu().pin_memory(), l.w.cpu().pin_memory(), l.dy.cpu().pin_memory(),
+                l.bias.cpu().pin_memory()) for l in lins]
+    host_out = [(torch.empty_like(l.y, device="cpu").pin_memory(), torch.empty_like(l.dx, device="cpu").pin_memory(),
+                 torch.empty_like(l.dw, device="cpu").pin_memory()) for l in lins]
+    h2d = sum(t.numel() * t.element_size() for tup in host_in for t in tup)
+    d2h = sum(t.numel() * t.element_size() for tup in host_out for t in tup)
+
+    def step():
+        for l, (x, w, dy, b) in zip(lins, host_in):
+            l.x.copy_(x, non_blocking=True)
+            l.w.copy_(w, non_blocking=True)
+            l.dy.copy_(dy, non_blocking=True)
+            l.bias.copy_(b, non_blocking=True)
+        layer.run(HEADLINE[0], autocast=True)
+        for l, (y, dx, dw) in zip(lins, host_out):
+            y.copy_(l.y, non_blocking=True)
+            dx.copy_(l.dx, non_blocking=True)
+            dw.copy_(l.dw, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), ws) / args.e2e_steps / ws
+    return {"value": round(ms, 4), "unit": "ms/layer", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "recipe": HEADLINE[0], "steps": args.e2e_steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -190,9 +190,17 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
  * M, N, K multiples of 16 (K of 32 for NVFP4).  Timing of the GEMM alone is the
  * pages' "pre-quantized" mode; quantize + GEMM is "autocast" mode. */
 
-/* BF16 x BF16 (kind::f16), alpha = 1. */
-te_status te_gemm_bf16(const void* A, const void* B, const float* bias, void* D, te_dtype out_dtype,
-                       int64_t M, int64_t N, int64_t K, void* stream);
+/* Operand storage order for te_gemm_bf16. */
+typedef enum {
+  TE_K_MAJOR = 0,  /* A stored [M, K] / B stored [N, K] (contraction contiguous) */
+  TE_MN_MAJOR = 1  /* A stored [K, M] / B stored [K, N] (the non-contracted index contiguous) */
+} te_layout;
+
+/* BF16 x BF16 (kind::f16), alpha = 1.  Each operand may be stored either way, so
+ * Dgrad (dX = dY W: B = W read MN-major) and Wgrad (dW = dY^T X: both operands
+ * MN-major) need no transposed copies, as a BF16 layer has none. */
+te_status te_gemm_bf16(const void* A, te_layout a_layout, const void* B, te_layout b_layout, const float* bias,
+                       void* D, te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* Per-tensor scaled FP8 (kind::f8f6f4): fa, fb in {TE_E4M3, TE_E5M2};
  * alpha = a_scale_inv[0] * b_scale_inv[0] (device fp32 scalars). */

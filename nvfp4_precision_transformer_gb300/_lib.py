@@ -21,6 +21,8 @@ F32, BF16, E4M3, E5M2, E2M1, E8M0, UE4M3 = range(7)
 # NVFP4 flags
 NVFP4_2D, NVFP4_RHT_COL, NVFP4_SR = 1, 2, 4
 ALGO_MAX, ALGO_MOST_RECENT = 0, 1
+# te_layout
+K_MAJOR, MN_MAJOR = 0, 1
 
 STATUS = {0: "TE_OK", 1: "TE_ERR_NULL", 2: "TE_ERR_SHAPE", 3: "TE_ERR_ALIGN", 4: "TE_ERR_DTYPE",
           5: "TE_ERR_UNSUPPORTED", 6: "TE_ERR_CUDA", 7: "TE_ERR_TIMEOUT", 8: "TE_ERR_ARG"}
@@ -42,7 +44,7 @@ SIGNATURES = {
     "te_quantize_mxfp8": (_st, [_vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "te_quantize_nvfp4": (_st, [_vp, _int, _i64, _i64, _u32, _u32, _u64, _u64, _vp, _vp,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "te_gemm_bf16": (_st, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
+    "te_gemm_bf16": (_st, [_vp, _int, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
     "te_gemm_fp8": (_st, [_vp, _int, _vp, _int, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
     "te_gemm_mxfp8": (_st, [_vp, _int, _vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
     "te_gemm_nvfp4": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
@@ -165,11 +167,12 @@ def _out_dtype(d):
     raise TypeError(f"unsupported output dtype {d.dtype}")
 
 
-def te_gemm_bf16(A, B, D, bias=None, stream=None):
-    M, K = A.shape
-    N = B.shape[0]
-    _check("te_gemm_bf16", lib().te_gemm_bf16(_ptr(A), _ptr(B), _ptr(bias), _ptr(D), _out_dtype(D), M, N, K,
-                                              _stream(stream)))
+def te_gemm_bf16(A, B, D, bias=None, a_layout: int = 0, b_layout: int = 0, stream=None):
+    """A is [M, K] (K_MAJOR) or [K, M] (MN_MAJOR); B is [N, K] or [K, N]; D is [M, N]."""
+    M, N = D.shape
+    K = A.shape[1] if a_layout == K_MAJOR else A.shape[0]
+    _check("te_gemm_bf16", lib().te_gemm_bf16(_ptr(A), a_layout, _ptr(B), b_layout, _ptr(bias), _ptr(D),
+                                              _out_dtype(D), M, N, K, _stream(stream)))
 
 
 def te_gemm_fp8(A, fa: int, B, fb: int, a_scale_inv, b_scale_inv, D, bias=None, stream=None):

@@ -77,6 +77,7 @@ struct GemmArgs {
   void* D;
   int out_f32;
   uint32_t idesc;
+  int a_mn, b_mn;       // BF16 only: operand stored [K, M] / [K, N]
   int* err;
 };
 
@@ -162,8 +163,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             bytes += sfb_halves * C::kSfAtoms * 512;
           }
           dev::mbar_expect_tx(&full[stage], bytes);
-          dev::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, mt * BM);
-          dev::tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, nt * BN);
+          if (KIND == kBF16 && args.a_mn) {
+            // [K, M] storage: 64 K-rows x 64 M-elements (128 B) per box, two boxes along M
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h)
+              dev::tma_load_2d(sA + stage * C::kABytes + h * 8192, &tmA, &full[stage], (mt * BM + 64 * h) * 2, kt * 64);
+          } else {
+            dev::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, mt * BM);
+          }
+          if (KIND == kBF16 && args.b_mn) {
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h)
+              dev::tma_load_2d(sB + stage * C::kBBytes + h * 8192, &tmB, &full[stage], (nt * BN + 64 * h) * 2, kt * 64);
+          } else {
+            dev::tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, nt * BN);
+          }
           if (C::kBlockScaled) {
             const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
             dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
@@ -228,8 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t adesc = dev::smem_desc(a_addr + 32 * ks, 0, 1024, 2);
-            const uint64_t bdesc = dev::smem_desc(b_addr + 32 * ks, 0, 1024, 2);
+            // K-major: 128-byte rows, 8-row swizzle atoms 1024 B apart; a k-step advances 32 B.
+            // MN-major (BF16): 64-element x 8-K-row atoms, 1024 B apart along K (SBO) and
+            // 8 KB apart along M / N (LBO); a k-step of 16 K-rows advances 2048 B.
+            const uint64_t adesc = (KIND == kBF16 && args.a_mn) ? dev::smem_desc(a_addr + 2048 * ks, 8192, 1024, 2)
+                                                                : dev::smem_desc(a_addr + 32 * ks, 0, 1024, 2);
+            const uint64_t bdesc = (KIND == kBF16 && args.b_mn) ? dev::smem_desc(b_addr + 2048 * ks, 8192, 1024, 2)
+                                                                : dev::smem_desc(b_addr + 32 * ks, 0, 1024, 2);
             const uint32_t acc = (kt | ks) != 0;
             if (KIND == kBF16) {
               dev::mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
@@ -340,7 +359,8 @@ uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt) {
 template <int KIND>
 te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
                       int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
-                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st) {
+                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
+                      int a_mn = 0, int b_mn = 0) {
   using C = Cfg<KIND>;
   static bool attr_set[64] = {false};
   int dev_id = 0;
@@ -352,9 +372,11 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
     attr_set[dev_id] = true;
   }
   CUtensorMap ta, tb;
-  te_status s = make_tmap_2d(&ta, A, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(M), BM);
+  te_status s = a_mn ? make_tmap_2d(&ta, A, static_cast<uint64_t>(M) * 2, static_cast<uint64_t>(K), 64)
+                     : make_tmap_2d(&ta, A, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(M), BM);
   if (s != TE_OK) return s;
-  s = make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
+  s = b_mn ? make_tmap_2d(&tb, B, static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K), 64)
+           : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
   if (s != TE_OK) return s;
   int* err = device_error_word();
   if (err == nullptr) return record_cuda(cudaErrorInvalidDevice);
@@ -374,7 +396,9 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.bias = bias;
   g.D = D;
   g.out_f32 = out == TE_F32;
-  g.idesc = make_idesc(KIND, afmt, bfmt);
+  g.idesc = make_idesc(KIND, afmt, bfmt) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
   g.err = err;
   const int tiles = g.m_tiles * g.n_tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
@@ -404,12 +428,14 @@ using namespace te;
 
 extern "C" {
 
-te_status te_gemm_bf16(const void* A, const void* B, const float* bias, void* D, te_dtype out_dtype, int64_t M,
-                       int64_t N, int64_t K, void* stream) {
+te_status te_gemm_bf16(const void* A, te_layout a_layout, const void* B, te_layout b_layout, const float* bias, void* D,
+                       te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream) {
+  if ((a_layout != TE_K_MAJOR && a_layout != TE_MN_MAJOR) || (b_layout != TE_K_MAJOR && b_layout != TE_MN_MAJOR))
+    return TE_ERR_ARG;
   te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
   if (s != TE_OK || M * N == 0) return s;
   return launch_gemm<kBF16>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, M, N, K, 1u, 1u,
-                            static_cast<cudaStream_t>(stream));
+                            static_cast<cudaStream_t>(stream), a_layout == TE_MN_MAJOR, b_layout == TE_MN_MAJOR);
 }
 
 te_status te_gemm_fp8(const uint8_t* A, te_dtype fa, const uint8_t* B, te_dtype fb, const float* a_scale_inv,

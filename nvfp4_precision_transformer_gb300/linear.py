@@ -1,0 +1,230 @@
+"""The quantized linear layer Y = X W^T + b as sequences of C-ABI calls.
+
+For each recipe the three GEMMs of a linear are issued in the pages' autocast
+mode -- both operands are quantized, in the orientation that GEMM consumes,
+right before it -- or in pre-quantized mode (the GEMM alone on operands
+quantized earlier).  ("How to Optimize Transformer-Based Models for
+Low-Precision Training", section "autocast モードの使用と事前量子化の比較"; the
+NVFP4 extras -- RHT on Wgrad inputs, SR on gradients, 2D weight blocks, the
+extra amax pass -- from section "実モデルにおける結果の解釈".)
+
+Recipes
+  bf16         BF16 GEMMs, no quantization (Dgrad / Wgrad read operands MN-major)
+  fp8_delayed  per-tensor FP8, scale from the amax history (HYBRID: E4M3 X/W, E5M2 dY)
+  fp8_current  per-tensor FP8, scale from the tensor's own amax (extra amax pass)
+  mxfp8        1x32 E8M0-scaled E4M3 blocks along the contraction
+  nvfp4        1x16 UE4M3-scaled E2M1 blocks; X/dY col copies rotated (RHT),
+               dY stochastically rounded, W in 16x16 blocks
+
+Everything here is marshalling: device buffers (torch allocations) and the
+order of launches; all arithmetic runs in libte_gb300.so.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+RECIPES = ("bf16", "fp8_delayed", "fp8_current", "mxfp8", "nvfp4")
+PASSES = ("fprop", "dgrad", "wgrad")
+
+
+class DelayedState:
+    """DelayedScaling state of a group of tensors: amax history ring, scale, scale_inv, last amax."""
+
+    def __init__(self, n: int, history_len: int, device):
+        self.n, self.L = n, history_len
+        self.hist = torch.zeros(n * history_len, dtype=torch.float32, device=device)
+        self.scale = torch.ones(n, dtype=torch.float32, device=device)
+        self.scale_inv = torch.ones(n, dtype=torch.float32, device=device)
+        self.amax = torch.zeros(n, dtype=torch.float32, device=device)
+
+    def slot(self, i: int):
+        return self.scale[i:i + 1], self.scale_inv[i:i + 1], self.amax[i:i + 1]
+
+
+class QuantLinear:
+    """Device buffers of one linear (inputs, outputs, quantized copies) and its GEMM passes."""
+
+    def __init__(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, bias: torch.Tensor | None,
+                 recipes=RECIPES, rht_signs: int = 0, sr_seed: int = 0, fwd_state: DelayedState | None = None,
+                 fwd_slots=(0, 1), bwd_state: DelayedState | None = None, bwd_slot: int = 0):
+        dev = x.device
+        self.x, self.w, self.dy, self.bias = x, w, dy, bias
+        M, Kin = x.shape
+        Nout = w.shape[0]
+        self.M, self.Kin, self.Nout = M, Kin, Nout
+        self.rht_signs, self.sr_seed, self.sr_offset = rht_signs, sr_seed, 0
+        bf = torch.bfloat16
+        self.y = torch.empty(M, Nout, dtype=bf, device=dev)
+        self.dx = torch.empty(M, Kin, dtype=bf, device=dev)
+        self.dw = torch.empty(Nout, Kin, dtype=bf, device=dev)
+        u8 = dict(dtype=torch.uint8, device=dev)
+
+        def f32():
+            return torch.zeros(1, dtype=torch.float32, device=dev)
+
+        # FP8 / MXFP8 copies (shared by the three 8-bit recipes)
+        if any(r in recipes for r in ("fp8_delayed", "fp8_current", "mxfp8")):
+            self.xr, self.xc = torch.empty(M, Kin, **u8), torch.empty(Kin, M, **u8)
+            self.wr, self.wc = torch.empty(Nout, Kin, **u8), torch.empty(Kin, Nout, **u8)
+            self.dr, self.dc = torch.empty(M, Nout, **u8), torch.empty(Nout, M, **u8)
+        if "fp8_current" in recipes:
+            self.cur = {k: (f32(), f32()) for k in ("x", "w", "dy")}    # (amax, scale_inv)
+        if "fp8_delayed" in recipes:
+            assert fwd_state is not None and bwd_state is not None
+            self.dl = {"x": fwd_state.slot(fwd_slots[0]), "w": fwd_state.slot(fwd_slots[1]),
+                       "dy": bwd_state.slot(bwd_slot)}
+        if "mxfp8" in recipes:
+            def sb(r, c):
+                return torch.zeros(L.te_scale_bytes(L.E8M0, r, c), **u8)
+            self.sxr, self.sxc = sb(M, Kin), sb(Kin, M)
+            self.swr, self.swc = sb(Nout, Kin), sb(Kin, Nout)
+            self.sdr, self.sdc = sb(M, Nout), sb(Nout, M)
+        if "nvfp4" in recipes:
+            def nb(r, c):
+                return (torch.empty(r, c // 2, **u8), torch.zeros(L.te_scale_bytes(L.UE4M3, r, c), **u8), f32())
+            self.nxr, self.nxc = nb(M, Kin), nb(Kin, M)
+            self.nwr, self.nwc = nb(Nout, Kin), nb(Kin, Nout)
+            self.ndr, self.ndc = nb(M, Nout), nb(Nout, M)
+            self.namax = {k: (f32(), f32()) for k in ("x", "w", "dy")}  # (amax, amax after RHT)
+
+    # ---- quantizers (one orientation each, as autocast does per GEMM) -----------------------
+    def _q_fp8(self, recipe, name, t, fmt, row=None, col=None):
+        if recipe == "fp8_current":
+            amax, sinv = self.cur[name]
+            L.te_quantize_fp8(t, fmt, None, 1, row, col, amax, sinv)
+        else:
+            scale, _, amax = self.dl[name]
+            L.te_quantize_fp8(t, fmt, scale, 0, row, col, amax, None)
+
+    def _sinv(self, recipe, name):
+        return self.cur[name][1] if recipe == "fp8_current" else self.dl[name][1]
+
+    def _q_nv(self, name, t, flags, row=None, col=None, rotated=False):
+        amax, amax_rht = self.namax[name]
+        L.te_amax_reduce(t, amax, amax_rht if rotated else None, self.rht_signs)
+        rq = row if row is not None else (None, None, None)
+        cq = col if col is not None else (None, None, None)
+        L.te_quantize_nvfp4(t, flags, self.rht_signs, self.sr_seed, self.sr_offset, amax, amax_rht,
+                            rq[0], rq[1], rq[2], cq[0], cq[1], cq[2])
+
+    def quantize(self, recipe: str, pass_: str) -> None:
+        """Quantize the two operands of one GEMM (autocast: right before the GEMM)."""
+        if recipe == "bf16":
+            return
+        E4, E5 = L.E4M3, L.E5M2
+        if recipe in ("fp8_current", "fp8_delayed"):
+            if pass_ == "fprop":
+                self._q_fp8(recipe, "x", self.x, E4, row=self.xr)
+                self._q_fp8(recipe, "w", self.w, E4, row=self.wr)
+            elif pass_ == "dgrad":
+                self._q_fp8(recipe, "dy", self.dy, E5, row=self.dr)
+                self._q_fp8(recipe, "w", self.w, E4, col=self.wc)
+            else:
+                self._q_fp8(recipe, "dy", self.dy, E5, col=self.dc)
+                self._q_fp8(recipe, "x", self.x, E4, col=self.xc)
+        elif recipe == "mxfp8":
+            if pass_ == "fprop":
+                L.te_quantize_mxfp8(self.x, self.xr, self.sxr)
+                L.te_quantize_mxfp8(self.w, self.wr, self.swr)
+            elif pass_ == "dgrad":
+                L.te_quantize_mxfp8(self.dy, self.dr, self.sdr)
+                L.te_quantize_mxfp8(self.w, None, None, self.wc, self.swc)
+            else:
+                L.te_quantize_mxfp8(self.dy, None, None, self.dc, self.sdc)
+                L.te_quantize_mxfp8(self.x, None, None, self.xc, self.sxc)
+        elif recipe == "nvfp4":
+            RHT, SR, D2 = L.NVFP4_RHT_COL, L.NVFP4_SR, L.NVFP4_2D
+            if pass_ == "fprop":
+                self._q_nv("x", self.x, 0, row=self.nxr)
+                self._q_nv("w", self.w, D2, row=self.nwr)
+            elif pass_ == "dgrad":
+                self._q_nv("dy", self.dy, SR, row=self.ndr)
+                self._q_nv("w", self.w, D2, col=self.nwc)
+            else:
+                self._q_nv("dy", self.dy, RHT | SR, col=self.ndc, rotated=True)
+                self._q_nv("x", self.x, RHT, col=self.nxc, rotated=True)
+        else:
+            raise ValueError(recipe)
+
+    def gemm(self, recipe: str, pass_: str) -> None:
+        """The GEMM of one pass on already-quantized operands."""
+        E4, E5 = L.E4M3, L.E5M2
+        KM, MN = L.K_MAJOR, L.MN_MAJOR
+        if recipe == "bf16":
+            if pass_ == "fprop":
+                L.te_gemm_bf16(self.x, self.w, self.y, self.bias, KM, KM)
+            elif pass_ == "dgrad":
+                L.te_gemm_bf16(self.dy, self.w, self.dx, None, KM, MN)
+            else:
+                L.te_gemm_bf16(self.dy, self.x, self.dw, None, MN, MN)
+        elif recipe in ("fp8_current", "fp8_delayed"):
+            sx, sw, sd = (self._sinv(recipe, n) for n in ("x", "w", "dy"))
+            if pass_ == "fprop":
+                L.te_gemm_fp8(self.xr, E4, self.wr, E4, sx, sw, self.y, self.bias)
+            elif pass_ == "dgrad":
+                L.te_gemm_fp8(self.dr, E5, self.wc, E4, sd, sw, self.dx)
+            else:
+                L.te_gemm_fp8(self.dc, E5, self.xc, E4, sd, sx, self.dw)
+        elif recipe == "mxfp8":
+            if pass_ == "fprop":
+                L.te_gemm_mxfp8(self.xr, self.sxr, self.wr, self.swr, self.y, self.bias)
+            elif pass_ == "dgrad":
+                L.te_gemm_mxfp8(self.dr, self.sdr, self.wc, self.swc, self.dx)
+            else:
+                L.te_gemm_mxfp8(self.dc, self.sdc, self.xc, self.sxc, self.dw)
+        elif recipe == "nvfp4":
+            if pass_ == "fprop":
+                a, b, out, bias = self.nxr, self.nwr, self.y, self.bias
+            elif pass_ == "dgrad":
+                a, b, out, bias = self.ndr, self.nwc, self.dx, None
+            else:
+                a, b, out, bias = self.ndc, self.nxc, self.dw, None
+            L.te_gemm_nvfp4(a[0], a[1], a[2], b[0], b[1], b[2], out, bias)
+        else:
+            raise ValueError(recipe)
+
+    def gemm_shape(self, pass_: str):
+        if pass_ == "fprop":
+            return self.M, self.Nout, self.Kin
+        if pass_ == "dgrad":
+            return self.M, self.Kin, self.Nout
+        return self.Nout, self.Kin, self.M
+
+
+class Layer:
+    """The four linears of one transformer layer with shared DelayedScaling state."""
+
+    def __init__(self, tensors, recipes=RECIPES, history_len: int = 16, rht_signs: int = 0, sr_seed: int = 0,
+                 device="cuda"):
+        n = len(tensors)
+        self.recipes = recipes
+        self.fwd = DelayedState(2 * n, history_len, device)
+        self.bwd = DelayedState(n, history_len, device)
+        self.recipe = L.te_recipe(L.E4M3, L.E5M2, history_len, L.ALGO_MAX, 0, 1)
+        self.linears = [QuantLinear(x, w, dy, b, recipes, rht_signs, sr_seed, self.fwd, (2 * i, 2 * i + 1),
+                                    self.bwd, i) for i, (x, w, dy, b) in enumerate(tensors)]
+        self.step_idx = 0
+
+    def scale_update(self) -> None:
+        """DelayedScaling bookkeeping after a step: record amaxes, refresh scales (two launches)."""
+        L.te_scale_update(self.recipe, 0, self.fwd.hist, self.fwd.amax, self.fwd.scale, self.fwd.scale_inv,
+                          self.step_idx)
+        L.te_scale_update(self.recipe, 1, self.bwd.hist, self.bwd.amax, self.bwd.scale, self.bwd.scale_inv,
+                          self.step_idx)
+
+    def run(self, recipe: str, autocast: bool = True, on_gemm=None) -> None:
+        """One layer's 12 GEMMs; ``on_gemm(lin, pass_, phase)`` brackets each GEMM launch."""
+        for lin in self.linears:
+            lin.sr_offset = self.step_idx
+            for p in PASSES:
+                if autocast:
+                    lin.quantize(recipe, p)
+                if on_gemm:
+                    on_gemm(lin, p, 0)
+                lin.gemm(recipe, p)
+                if on_gemm:
+                    on_gemm(lin, p, 1)
+        if autocast and recipe == "fp8_delayed":
+            self.scale_update()

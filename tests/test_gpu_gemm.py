@@ -55,11 +55,14 @@ SMALL = [(272, 208, 528), (16, 32, 48), (1024, 768, 768), (384, 512, 256)]
 def test_bf16_three_passes(M, Kin, Nout, out):
     x, w, dy, b = _linear(M, Kin, Nout, 100)
     x32, w32, dy32 = G.f32_np(x), G.f32_np(w), G.f32_np(dy)
-    passes = [("fprop", x, w, x32, w32, b), ("dgrad", dy, w.t().contiguous(), dy32, w32.T, None),
-              ("wgrad", dy.t().contiguous(), x.t().contiguous(), dy32.T, x32.T, None)]
-    for name, A, B, A32, B32, bias in passes:
-        D = torch.empty(A.shape[0], B.shape[0], dtype=out, device=G.DEV)
-        te.te_gemm_bf16(A, B, D, bias)
+    KM, MN = te.K_MAJOR, te.MN_MAJOR
+    # dgrad reads W [Nout, Kin] as B stored [K, N]; wgrad reads dY and X as stored [K, M] / [K, N]
+    passes = [("fprop", x, KM, w, KM, x32, w32, b, (M, Nout)), ("dgrad", dy, KM, w, MN, dy32, w32.T, None, (M, Kin)),
+              ("wgrad", dy, MN, x, MN, dy32.T, x32.T, None, (Nout, Kin)),
+              ("fprop-transposed-copies", x, KM, w.t().contiguous(), MN, x32, w32, b, (M, Nout))]
+    for name, A, la, B, lb, A32, B32, bias, dshape in passes:
+        D = torch.empty(*dshape, dtype=out, device=G.DEV)
+        te.te_gemm_bf16(A, B, D, bias, a_layout=la, b_layout=lb)
         torch.cuda.synchronize()
         ref = OG.gemm(A32, B32, bias=None if bias is None else b.cpu().numpy())
         _cmp(D, ref, f"bf16 {name}")
@@ -313,5 +316,5 @@ def test_gemm_rejects_bad_shapes():
     A = torch.zeros(32, 40, dtype=torch.bfloat16, device=G.DEV)
     D = torch.empty(32, 32, dtype=torch.float32, device=G.DEV)
     with pytest.raises(te.TEError) as ei:
-        te.te_gemm_bf16(A, torch.zeros(32, 40, dtype=torch.bfloat16, device=G.DEV), D)
+        te.te_gemm_bf16(A, torch.zeros(32, 40, dtype=torch.bfloat16, device=G.DEV), D)   # K = 40
     assert ei.value.status == 2
