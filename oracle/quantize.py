@@ -29,7 +29,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import formats as F
-from .philox import element_words
+from .philox import element_rand16
 
 f32 = np.float32
 
@@ -152,13 +152,14 @@ def nvfp4_global(tensor_amax):
     return s, f32(f32(1.0) / s)
 
 
-def e2m1_round_stochastic(v, words) -> np.ndarray:
+def e2m1_round_stochastic(v, rand16) -> np.ndarray:
     """Stochastic rounding of fp32 values v to E2M1 codes.
 
     |v| >= 6 saturates to 6.  Otherwise lo is the largest E2M1 magnitude <= |v|,
     hi the next one, and frac = (|v| - lo) / (hi - lo) (exact in fp32: the
     difference is exact by Sterbenz or lo = 0, the spacing is a power of two).
-    The magnitude rounds up iff (word >> 8) * 2**-24 < frac.  The sign is kept.
+    The magnitude rounds up iff rand16 * 2**-16 < frac (rand16: a 16-bit
+    uniform integer per element).  The sign is kept.
     """
     v = np.asarray(v, dtype=np.float32)
     a = np.abs(v)
@@ -168,8 +169,8 @@ def e2m1_round_stochastic(v, words) -> np.ndarray:
     hi = E2M1_GRID[np.minimum(idx + 1, 7)]
     span = np.where(idx < 7, hi - lo, f32(1.0)).astype(np.float32)
     frac = ((a - lo).astype(np.float32) / span).astype(np.float32)
-    k = (np.asarray(words, dtype=np.uint32) >> 8).astype(np.float64)
-    up = (k * 2.0 ** -24) < frac.astype(np.float64)
+    k = (np.asarray(rand16, dtype=np.uint32) & 0xFFFF).astype(np.float64)
+    up = (k * 2.0 ** -16) < frac.astype(np.float64)
     mag = np.where(a >= 6.0, f32(6.0), np.where(up & (idx < 7), hi, lo)).astype(np.float32)
     signed = np.where(np.signbit(v), -mag, mag).astype(np.float32)
     return F.encode(signed, "e2m1")
@@ -209,8 +210,8 @@ def nvfp4_quantize(z, tensor_amax, block2d: bool = False, sr=None):
     if sr is None:
         q = F.encode(v, "e2m1")
     else:
-        words = element_words(R * C, sr["row0"] * sr["cols"], sr["seed"], sr["copy_id"], sr["offset"])
-        q = e2m1_round_stochastic(v, words.reshape(R, C))
+        r16 = element_rand16(R * C, sr["row0"] * sr["cols"], sr["seed"], sr["copy_id"], sr["offset"])
+        q = e2m1_round_stochastic(v, r16.reshape(R, C))
     return q, s_codes, s_dec
 
 

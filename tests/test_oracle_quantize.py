@@ -198,10 +198,10 @@ def test_pack_unpack_nibble_order():
 
 def test_sr_exact_values_never_move_and_neighbours_only():
     grid = np.concatenate([Q.E2M1_GRID, -Q.E2M1_GRID]).astype(np.float32)
-    words = rng.integers(0, 1 << 32, size=grid.size, dtype=np.uint64).astype(np.uint32)
+    words = rng.integers(0, 1 << 16, size=grid.size, dtype=np.uint64).astype(np.uint32)
     np.testing.assert_array_equal(Q.e2m1_round_stochastic(grid, words), F.encode(grid, "e2m1"))
     v = rng.uniform(-7, 7, size=4096).astype(np.float32)
-    words = rng.integers(0, 1 << 32, size=v.size, dtype=np.uint64).astype(np.uint32)
+    words = rng.integers(0, 1 << 16, size=v.size, dtype=np.uint64).astype(np.uint32)
     got = F.decode(Q.e2m1_round_stochastic(v, words), "e2m1")
     a = np.minimum(np.abs(v), 6.0)
     lo = Q.E2M1_GRID[np.clip(np.searchsorted(Q.E2M1_GRID, a, side="right") - 1, 0, 7)]
@@ -211,19 +211,22 @@ def test_sr_exact_values_never_move_and_neighbours_only():
 
 
 def test_sr_threshold_rule():
-    # frac = 0.25 at v = 2.25 (between 2 and 3): up iff (w >> 8) < 0.25 * 2**24
+    # frac = 0.25 at v = 2.25 (between 2 and 3): up iff r16 < 0.25 * 2**16
     v = np.full(4, 2.25, np.float32)
-    w = np.array([0, (1 << 22) - 1, 1 << 22, 0xFFFFFFFF], np.uint64) << np.uint64(8)
-    w = (w & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    w = np.array([0, (1 << 14) - 1, 1 << 14, 0xFFFF], np.uint32)
     got = F.decode(Q.e2m1_round_stochastic(v, w), "e2m1")
     assert list(got) == [3.0, 3.0, 2.0, 2.0]
+    # tiny fraction: only r16 = 0 rounds up
+    v = np.full(2, 4.0 + 2.0 ** -20, np.float32)
+    got = F.decode(Q.e2m1_round_stochastic(v, np.array([0, 1], np.uint32)), "e2m1")
+    assert list(got) == [6.0, 4.0]
 
 
 @pytest.mark.parametrize("v", [0.1, 0.8, 1.3, 2.6, 3.3, 4.9, 5.99])
 def test_sr_unbiased(v):
     n = 1 << 18
-    from oracle.philox import element_words
-    words = element_words(n, 0, seed=977, copy_id=0, offset=int(v * 100))
+    from oracle.philox import element_rand16
+    words = element_rand16(n, 0, seed=977, copy_id=0, offset=int(v * 100))
     got = F.decode(Q.e2m1_round_stochastic(np.full(n, v, np.float32), words), "e2m1")
     lo = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v) - 1]
     hi = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v)]
