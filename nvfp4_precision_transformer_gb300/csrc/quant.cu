@@ -3,13 +3,12 @@
 // MXFP8 and NVFP4 quantizers that write the row-wise and column-wise
 // (transposed) copies of a tensor from a single read.
 //
-// Every quantizer works on 64 x 64 tiles staged once in shared memory as fp32:
-// the row copy is produced from tile rows, the col copy from tile columns, so
-// the input is read from HBM exactly once.  Loads are 16-byte vectors, coalesced
-// along the row; stores of both copies are 16-byte (FP8/MXFP8) or 8-byte (NVFP4)
-// vectors.  All code-deciding arithmetic is IEEE fp32 round-to-nearest-even
-// (compiled with -fmad=false) so the codes are bit-identical to the definitions
-// in te_gb300.h.
+// Every quantizer thread owns a register patch (16 or 32 consecutive rows of one
+// 16- or 8-byte row vector), so the input is read from HBM exactly once for both
+// copies, with all of a thread's loads in flight together and no shared-memory
+// staging or block barriers.  All code-deciding arithmetic is IEEE fp32
+// round-to-nearest-even (compiled with -fmad=false) so the codes are bit-identical
+// to the definitions in te_gb300.h.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -18,26 +17,7 @@
 namespace te {
 namespace {
 
-constexpr int kTile = 64;
 constexpr int kThreads = 256;
-
-// ---- element access ----------------------------------------------------------------
-
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 
 // ---- format conversions (hardware cvt, round-to-nearest-even, satfinite) --------------
 
@@ -96,8 +76,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 // Stochastic rounding of v to E2M1: the magnitude moves up to the next grid
-// point iff (w >> 8) * 2^-24 < (|v| - lo) / (hi - lo); |v| >= 6 saturates.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t w) {
+// point iff r16 * 2^-16 < (|v| - lo) / (hi - lo); |v| >= 6 saturates.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
   const float a = fabsf(v);
   const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
   if (a >= 6.0f) return sign | 7u;
@@ -111,7 +91,7 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t w) {
   else if (a < 4.0f) { lo = 3.0f; inv_span = 1.0f; code = 5; }
   else { lo = 4.0f; inv_span = 0.5f; code = 6; }
   const float frac = __fmul_rn(__fsub_rn(a, lo), inv_span);  // exact
-  const float thr = __fmul_rn(static_cast<float>(w >> 8), 5.9604644775390625e-8f);  // exact: k * 2^-24
+  const float thr = __fmul_rn(static_cast<float>(r16), 1.52587890625e-5f);  // exact: r16 * 2^-16
   return sign | (thr < frac ? code + 1u : code);
 }
 
@@ -142,6 +122,13 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
+// Max over aligned groups of L consecutive lanes (L a power of two <= 32).
+template <int L>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
 // Block-wide max, then one atomicMax on the (non-negative) fp32 bit pattern.
 __device__ __forceinline__ void block_max_to(float v, float* out) {
   __shared__ float red[32];
@@ -154,43 +141,118 @@ __device__ __forceinline__ void block_max_to(float v, float* out) {
     v = warp_max(v);
     if (l == 0) atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(v));
   }
+  __syncthreads();
+}
+
+// ---- register patches ---------------------------------------------------------------------------
+// Every quantizer thread owns a patch of PR consecutive rows x one BYTES-wide vector
+// of a row (8 bf16 / 4 fp32 for 16 bytes).  Consecutive threads take consecutive
+// vectors of the same rows, so each of the PR loads is coalesced across the warp,
+// and all PR loads are issued before any arithmetic (PR x BYTES bytes in flight per
+// thread).  The row copy is produced row by row from the registers; the col copy
+// column by column -- PR consecutive rows are exactly one column block (NVFP4: 16,
+// MXFP8: 32), so no shared-memory transpose is needed.
+
+template <typename T, int BYTES>
+struct Chunk;
+template <>
+struct Chunk<__nv_bfloat16, 16> {
+  using Raw = uint4;
+  static constexpr int N = 8;
+};
+template <>
+struct Chunk<float, 16> {
+  using Raw = uint4;
+  static constexpr int N = 4;
+};
+template <>
+struct Chunk<__nv_bfloat16, 8> {
+  using Raw = uint2;
+  static constexpr int N = 4;
+};
+template <>
+struct Chunk<float, 8> {
+  using Raw = uint2;
+  static constexpr int N = 2;
+};
+
+__device__ __forceinline__ uint4 ld_raw(const uint4* p) { return __ldg(p); }
+__device__ __forceinline__ uint2 ld_raw(const uint2* p) { return __ldg(p); }
+__device__ __forceinline__ void zero_raw(uint4& r) { r = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero_raw(uint2& r) { r = make_uint2(0, 0); }
+__device__ __forceinline__ uint32_t raw_word(const uint4& r, int k) {
+  return k == 0 ? r.x : (k == 1 ? r.y : (k == 2 ? r.z : r.w));
+}
+__device__ __forceinline__ uint32_t raw_word(const uint2& r, int k) { return k == 0 ? r.x : r.y; }
+
+template <typename T, typename Raw>
+__device__ __forceinline__ float elem(const Raw& r, int i) {
+  if (sizeof(T) == 2) {
+    const uint32_t w = raw_word(r, i >> 1);
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+  return __uint_as_float(raw_word(r, i));
+}
+
+template <typename T, int BYTES, int PR>
+struct Patch {
+  using Ch = Chunk<T, BYTES>;
+  using Raw = typename Ch::Raw;
+  static constexpr int PC = Ch::N;
+  Raw raw[PR];
+  int64_t r0, c0;
+  bool live;
+
+  __device__ __forceinline__ void load(const T* __restrict__ x, int64_t R, int64_t C) {
+    const int64_t ncg = C / PC;
+    const int64_t total = (R / PR) * ncg;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    live = idx < total;
+    const int64_t band = live ? idx / ncg : 0;
+    r0 = band * PR;
+    c0 = live ? (idx - band * ncg) * PC : 0;
+    const T* p = x + r0 * C + c0;
+#pragma unroll
+    for (int r = 0; r < PR; ++r) {
+      if (live) raw[r] = ld_raw(reinterpret_cast<const Raw*>(p + r * C));
+      else zero_raw(raw[r]);
+    }
+  }
+  __device__ __forceinline__ float at(int r, int i) const { return elem<T>(raw[r], i); }
+  __device__ __forceinline__ float absmax() const {
+    float m = 0.0f;
+#pragma unroll
+    for (int r = 0; r < PR; ++r)
+#pragma unroll
+      for (int i = 0; i < PC; ++i) m = fmaxf(m, fabsf(at(r, i)));
+    return m;
+  }
+};
+
+inline unsigned patch_blocks(int64_t rows, int64_t cols, int pr, int pc) {
+  const int64_t total = (rows / pr) * (cols / pc);
+  const int64_t b = (total + kThreads - 1) / kThreads;
+  return static_cast<unsigned>(b < 1 ? 1 : b);
 }
 
 // ---- amax ---------------------------------------------------------------------------------------
-// Each thread reads a 16-row x 8-column patch (sixteen coalesced 16-byte loads),
-// takes the plain amax and, with RHT, the amax of the 8 transformed columns.
 template <typename T, bool RHT>
-__global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C, float* amax,
+__global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C, float* amax,
                                                         float* amax_rht, uint32_t signs) {
-  const int64_t ncg = C / 8;
-  const int64_t total = (R / 16) * ncg;
-  float m = 0.0f, mr = 0.0f;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t band = idx / ncg, cg = idx - band * ncg;
-    const T* p = x + band * 16 * C + cg * 8;
-    float v[16][8];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) load8(p + r * C, v[r]);
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(v[r][c]));
-    if (RHT) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float col[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) col[r] = v[r][c];
-        rht16(col, signs);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) mr = fmaxf(mr, fabsf(col[r]));
-      }
-    }
-  }
-  block_max_to(m, amax);
+  Patch<T, 16, 16> p;
+  p.load(x, R, C);
+  block_max_to(p.absmax(), amax);
   if (RHT) {
-    __syncthreads();
+    float mr = 0.0f;
+#pragma unroll
+    for (int i = 0; i < Patch<T, 16, 16>::PC; ++i) {
+      float col[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) col[r] = p.at(r, i);
+      rht16(col, signs);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) mr = fmaxf(mr, fabsf(col[r]));
+    }
     block_max_to(mr, amax_rht);
   }
 }
@@ -219,36 +281,6 @@ __global__ void scale_update_kernel(int n, int L, int algo, int interval, float 
   scale_inv[i] = __fdiv_rn(1.0f, s);
 }
 
-// ---- tile staging ---------------------------------------------------------------------------------
-// Loads the 64 x 64 tile at (r0, c0) into smem as fp32 (zeros outside [R, C]) and
-// returns the thread's partial amax.  Thread t loads rows t/8 and t/8 + 32,
-// columns (t % 8) * 8 .. + 7.
-template <typename T>
-__device__ __forceinline__ float stage_tile(const T* __restrict__ x, int64_t R, int64_t C, int64_t r0, int64_t c0,
-                                            float (*tile)[kTile + 1]) {
-  const int t = threadIdx.x;
-  const int cc = (t & 7) * 8;
-  float m = 0.0f;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int rr = (t >> 3) + 32 * h;
-    const int64_t r = r0 + rr, c = c0 + cc;
-    float v[8];
-    if (r < R && c < C) {
-      load8(x + r * C + c, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      tile[rr][cc + i] = v[i];
-      m = fmaxf(m, fabsf(v[i]));
-    }
-  }
-  return m;
-}
-
 __device__ __forceinline__ float current_scale(float a, float fmax) {
   if (!(isfinite(a) && a > 0.0f)) return 1.0f;
   const float s = __fdiv_rn(fmax, a);
@@ -268,36 +300,48 @@ struct Fp8Args {
   float* scale_inv_out;   // nullable
 };
 
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2(float a, float b) {
+  return E5M2 ? cvt_e5m2x2(a, b) : cvt_e4m3x2(a, b);
+}
+
 template <typename T, bool E5M2>
-__global__ void __launch_bounds__(kThreads) fp8_kernel(const T* __restrict__ x, Fp8Args a) {
-  __shared__ float tile[kTile][kTile + 1];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  const float lmax = stage_tile(x, a.R, a.C, r0, c0, tile);
+__global__ void __launch_bounds__(kThreads, 2) fp8_kernel(const T* __restrict__ x, Fp8Args a) {
+  using P = Patch<T, 16, 16>;
+  constexpr int PC = P::PC;
+  P p;
+  p.load(x, a.R, a.C);
   const float s = a.current ? current_scale(*a.amax_in, a.fmax) : *a.scale;
-  __syncthreads();
-  const int t = threadIdx.x;
-  const int lane_row = t >> 2, seg = (t & 3) * 16;
-  if (a.q_row != nullptr) {
-    const int64_t r = r0 + lane_row, c = c0 + seg;
-    if (r < a.R && c < a.C) {
-      float v[16];
+  if (p.live && a.q_row != nullptr) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = tile[lane_row][seg + i];
-      *reinterpret_cast<uint4*>(a.q_row + r * a.C + c) = pack_fp8_16<E5M2>(v, s);
+    for (int r = 0; r < 16; ++r) {
+      uint32_t w[PC / 4];
+#pragma unroll
+      for (int j = 0; j < PC / 4; ++j) {
+        const uint32_t lo = fp8x2<E5M2>(__fmul_rn(p.at(r, 4 * j), s), __fmul_rn(p.at(r, 4 * j + 1), s));
+        const uint32_t hi = fp8x2<E5M2>(__fmul_rn(p.at(r, 4 * j + 2), s), __fmul_rn(p.at(r, 4 * j + 3), s));
+        w[j] = lo | (hi << 16);
+      }
+      uint8_t* dst = a.q_row + (p.r0 + r) * a.C + p.c0;
+      if (PC == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[PC / 4 - 1]);
+      else *reinterpret_cast<uint32_t*>(dst) = w[0];
     }
   }
-  if (a.q_col != nullptr) {
-    const int64_t c = c0 + lane_row, r = r0 + seg;
-    if (c < a.C && r < a.R) {
-      float v[16];
+  if (p.live && a.q_col != nullptr) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = tile[seg + i][lane_row];
-      *reinterpret_cast<uint4*>(a.q_col + c * a.R + r) = pack_fp8_16<E5M2>(v, s);
+    for (int i = 0; i < PC; ++i) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = fp8x2<E5M2>(__fmul_rn(p.at(4 * j, i), s), __fmul_rn(p.at(4 * j + 1, i), s));
+        const uint32_t hi = fp8x2<E5M2>(__fmul_rn(p.at(4 * j + 2, i), s), __fmul_rn(p.at(4 * j + 3, i), s));
+        w[j] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(a.q_col + (p.c0 + i) * a.R + p.r0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  if (a.scale_inv_out != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && t == 0)
-    *a.scale_inv_out = __fdiv_rn(1.0f, s);
-  if (a.amax_out != nullptr) block_max_to(lmax, a.amax_out);
+  if (a.scale_inv_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.scale_inv_out = __fdiv_rn(1.0f, s);
+  if (a.amax_out != nullptr) block_max_to(p.absmax(), a.amax_out);
 }
 
 // ---- MXFP8 ----------------------------------------------------------------------------------------
@@ -310,6 +354,7 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   e -= 8;
   return max(-127, min(127, e));
 }
+__device__ __forceinline__ float mx_mult(int E) { return __uint_as_float(static_cast<uint32_t>(127 - E) << 23); }
 
 struct MxArgs {
   int64_t R, C;
@@ -321,53 +366,55 @@ struct MxArgs {
   int64_t kpad_col;
 };
 
-// One block of 32 is handled by two threads (16 elements each) that are lanes
-// t and t^1; it writes the codes and returns the scale byte.
-__device__ __forceinline__ uint32_t mx_quantize_half(const float (&v)[16], uint4* dst, bool valid) {
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
-  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-  const int E = mx_exponent(m);
-  const float mult = __uint_as_float(static_cast<uint32_t>(127 - E) << 23);
-  if (valid) *dst = pack_fp8_16<false>(v, mult);
-  return static_cast<uint32_t>(E + 127);
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads) mxfp8_kernel(const T* __restrict__ x, MxArgs a) {
-  __shared__ float tile[kTile][kTile + 1];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  stage_tile(x, a.R, a.C, r0, c0, tile);
-  __syncthreads();
-  const int t = threadIdx.x;
-  const int lane_row = t >> 2, sub = t & 3, seg = sub * 16;
+// PR = 32 when the col copy is requested (one column block per patch), else 16.
+template <typename T, int PR>
+__global__ void __launch_bounds__(kThreads, 2) mxfp8_kernel(const T* __restrict__ x, MxArgs a) {
+  using P = Patch<T, 8, PR>;
+  constexpr int PC = P::PC;
+  constexpr int LANES = 32 / PC;  // threads sharing one row block of 32
+  P p;
+  p.load(x, a.R, a.C);
   if (a.q_row != nullptr) {
-    const int64_t r = r0 + lane_row, c = c0 + seg;
-    const bool valid = r < a.R && c < a.C;
-    float v[16];
+    const bool first = ((p.c0 / PC) % LANES) == 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = tile[lane_row][seg + i];
-    const uint32_t sb = mx_quantize_half(v, reinterpret_cast<uint4*>(a.q_row + r * a.C + c), valid);
-    const uint32_t sb_next = __shfl_down_sync(0xFFFFFFFFu, sb, 2);  // block of columns 32..63
-    if (sub == 0 && r < a.R) {
-      const uint64_t j0 = static_cast<uint64_t>(c0 / 32);
-      const uint32_t hi = (c0 + 32 < a.C) ? sb_next : 0u;
-      *reinterpret_cast<uint16_t*>(a.s_row + scale_offset(r, j0, a.kpad_row)) = static_cast<uint16_t>(sb | (hi << 8));
+    for (int r = 0; r < PR; ++r) {
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < PC; ++i) m = fmaxf(m, fabsf(p.at(r, i)));
+      m = group_max<LANES>(m);
+      const int E = mx_exponent(m);
+      const float mult = mx_mult(E);
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < PC / 2; ++j)
+        w |= cvt_e4m3x2(__fmul_rn(p.at(r, 2 * j), mult), __fmul_rn(p.at(r, 2 * j + 1), mult)) << (16 * j);
+      if (p.live) {
+        uint8_t* dst = a.q_row + (p.r0 + r) * a.C + p.c0;
+        if (PC == 4) *reinterpret_cast<uint32_t*>(dst) = w;
+        else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+        if (first) a.s_row[scale_offset(p.r0 + r, p.c0 / 32, a.kpad_row)] = static_cast<uint8_t>(E + 127);
+      }
     }
   }
-  if (a.q_col != nullptr) {
-    const int64_t c = c0 + lane_row, r = r0 + seg;
-    const bool valid = c < a.C && r < a.R;
-    float v[16];
+  if (PR == 32 && a.q_col != nullptr && p.live) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = tile[seg + i][lane_row];
-    const uint32_t sb = mx_quantize_half(v, reinterpret_cast<uint4*>(a.q_col + c * a.R + r), valid);
-    const uint32_t sb_next = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-    if (sub == 0 && c < a.C) {
-      const uint64_t j0 = static_cast<uint64_t>(r0 / 32);
-      const uint32_t hi = (r0 + 32 < a.R) ? sb_next : 0u;
-      *reinterpret_cast<uint16_t*>(a.s_col + scale_offset(c, j0, a.kpad_col)) = static_cast<uint16_t>(sb | (hi << 8));
+    for (int i = 0; i < PC; ++i) {
+      float m = 0.0f;
+#pragma unroll
+      for (int r = 0; r < PR; ++r) m = fmaxf(m, fabsf(p.at(r, i)));
+      const int E = mx_exponent(m);
+      const float mult = mx_mult(E);
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(p.at(4 * j, i), mult), __fmul_rn(p.at(4 * j + 1, i), mult));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(p.at(4 * j + 2, i), mult), __fmul_rn(p.at(4 * j + 3, i), mult));
+        w[j] = lo | (hi << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.q_col + (p.c0 + i) * a.R + p.r0);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      a.s_col[scale_offset(p.c0 + i, p.r0 / 32, a.kpad_col)] = static_cast<uint8_t>(E + 127);
     }
   }
 }
@@ -395,113 +442,114 @@ __device__ __forceinline__ float nv_senc(float A) {
   return isfinite(s) ? s : 1.0f;
 }
 
-// Quantizes one 16-element block: returns the UE4M3 scale code, writes 8 packed bytes.
-// `g0` is the row-major index of v[0] inside the copy (for stochastic rounding).
-__device__ __forceinline__ uint32_t nv_quantize_block(const float (&v)[16], float blk_amax, float senc, bool sr,
-                                                      const NvArgs& a, uint32_t copy_id, uint64_t g0, uint2* dst,
-                                                      bool valid) {
-  const float pre = __fmul_rn(__fdiv_rn(blk_amax, 6.0f), senc);
-  const uint32_t sc = cvt_e4m3x2(pre, 0.0f) & 0x7Fu;
-  const float sv = ue4m3_value(sc);
-  const float r = sv > 0.0f ? __fdiv_rn(senc, sv) : 0.0f;
-  float y[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], r);
-  uint32_t lo = 0, hi = 0;
-  if (!sr) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) lo |= cvt_e2m1x2(y[2 * i], y[2 * i + 1]) << (8 * i);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hi |= cvt_e2m1x2(y[8 + 2 * i], y[8 + 2 * i + 1]) << (8 * i);
-  } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint64_t grp = (g0 >> 2) + q;
-      const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(grp), copy_id, a.off_lo, a.off_hi), a.seed_lo,
-                                    a.seed_hi);
-      const uint32_t n0 = e2m1_sr(y[4 * q], w.x), n1 = e2m1_sr(y[4 * q + 1], w.y);
-      const uint32_t n2 = e2m1_sr(y[4 * q + 2], w.z), n3 = e2m1_sr(y[4 * q + 3], w.w);
-      const uint32_t word16 = n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
-      if (q < 2) lo |= word16 << (16 * q);
-      else hi |= word16 << (16 * (q - 2));
-    }
-  }
-  if (valid) *dst = make_uint2(lo, hi);
-  return sc;
+// UE4M3 block-scale code of a block with amax bm: RN(fl32(fl32(bm / 6) * S_enc)).
+__device__ __forceinline__ uint32_t nv_scale_code(float bm, float senc) {
+  return cvt_e4m3x2(__fmul_rn(__fdiv_rn(bm, 6.0f), senc), 0.0f) & 0x7Fu;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) nvfp4_kernel(const T* __restrict__ x, NvArgs a) {
-  __shared__ float tile[kTile][kTile + 1];
-  __shared__ float amax2d[4][4];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  stage_tile(x, a.R, a.C, r0, c0, tile);
+// The 16-bit random values of the 8 elements g8*8 .. g8*8+7 of a copy (element
+// 2k + h takes half h of word k of Philox(counter = (g8, copy, offset))).
+__device__ __forceinline__ uint4 nv_rand8(const NvArgs& a, uint64_t g8, uint32_t copy_id) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(g8), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
+}
+__device__ __forceinline__ uint32_t rand16_of(const uint4& w, int k) {  // k = element index within the 8
+  const uint32_t word = raw_word(w, k >> 1);
+  return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+template <typename T, bool SR>
+__global__ void __launch_bounds__(kThreads, 2) nvfp4_kernel(const T* __restrict__ x, NvArgs a) {
+  using P = Patch<T, 16, 16>;
+  constexpr int PC = P::PC;
+  constexpr int LANES = 16 / PC;  // threads sharing one row block of 16
+  __shared__ float rtab[2][128];  // r = fl32(S_enc / dec(code)) for the row / col copy
+  const bool do_row = a.q_row != nullptr, do_col = a.q_col != nullptr;
+  const bool two_d = (a.flags & TE_NVFP4_2D) != 0, rht = (a.flags & TE_NVFP4_RHT_COL) != 0;
+  const float senc_r = do_row ? nv_senc(*a.amax) : 1.0f;
+  const float senc_c = do_col ? nv_senc(rht ? *a.amax_rht : *a.amax) : 1.0f;
+  if (threadIdx.x < 128) {
+    const float dv = ue4m3_value(threadIdx.x);
+    rtab[0][threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_r, dv) : 0.0f;
+    rtab[1][threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_c, dv) : 0.0f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (do_row && a.gdec_row != nullptr) *a.gdec_row = __fdiv_rn(1.0f, senc_r);
+    if (do_col && a.gdec_col != nullptr) *a.gdec_col = __fdiv_rn(1.0f, senc_c);
+  }
+  P p;
+  p.load(x, a.R, a.C);
   __syncthreads();
-  const int t = threadIdx.x;
-  const bool two_d = (a.flags & TE_NVFP4_2D) != 0;
-  const bool sr = (a.flags & TE_NVFP4_SR) != 0;
-  if (two_d) {
-    const int st = t >> 4, sr_ = st >> 2, sc_ = st & 3, rr = t & 15;
-    float m = 0.0f;
+  float tile_max = 0.0f;  // 2D: amax of the 16 x 16 tile this patch belongs to
+  if (two_d) tile_max = group_max<LANES>(p.absmax());
+
+  if (do_row) {
+    const bool first = ((p.c0 / PC) % LANES) == 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(tile[sr_ * 16 + rr][sc_ * 16 + i]));
+    for (int r = 0; r < 16; ++r) {
+      float m = 0.0f;
+      if (!two_d) {
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (rr == 0) amax2d[sr_][sc_] = m;
-    __syncthreads();
-  }
-  const int lane_row = t >> 2, sub = t & 3, seg = sub * 16;
-  if (a.q_row != nullptr) {
-    const float senc = nv_senc(*a.amax);
-    const int64_t r = r0 + lane_row, c = c0 + seg;
-    const bool valid = r < a.R && c < a.C;
-    float v[16];
+        for (int i = 0; i < PC; ++i) m = fmaxf(m, fabsf(p.at(r, i)));
+        m = group_max<LANES>(m);
+      } else {
+        m = tile_max;
+      }
+      const uint32_t sc = nv_scale_code(m, senc_r);
+      const float rr = rtab[0][sc];
+      const uint64_t g = static_cast<uint64_t>(p.r0 + r) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(p.c0);
+      uint32_t w = 0;
+      if (!SR) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = tile[lane_row][seg + i];
-    float bm = 0.0f;
-    if (two_d) {
-      bm = amax2d[lane_row >> 4][sub];
-    } else {
+        for (int j = 0; j < PC / 2; ++j)
+          w |= cvt_e2m1x2(__fmul_rn(p.at(r, 2 * j), rr), __fmul_rn(p.at(r, 2 * j + 1), rr)) << (8 * j);
+      } else {
+        const uint4 rnd = nv_rand8(a, g >> 3, 0u);
+        const int k0 = static_cast<int>(g & 7);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
+        for (int i = 0; i < PC; ++i) w |= e2m1_sr(__fmul_rn(p.at(r, i), rr), rand16_of(rnd, k0 + i)) << (4 * i);
+      }
+      if (p.live) {
+        uint8_t* dst = a.q_row + (p.r0 + r) * (a.C / 2) + p.c0 / 2;
+        if (PC == 8) *reinterpret_cast<uint32_t*>(dst) = w;
+        else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+        if (first) a.s_row[scale_offset(p.r0 + r, p.c0 / 16, a.kpad_row)] = static_cast<uint8_t>(sc);
+      }
     }
-    const uint64_t g0 = static_cast<uint64_t>(r) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(c);
-    const uint32_t sc = nv_quantize_block(v, bm, senc, sr, a, 0u, g0,
-                                          reinterpret_cast<uint2*>(a.q_row + r * (a.C / 2) + c / 2), valid);
-    uint32_t word = sc;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 1) << 8;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 2) << 16;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 3) << 24;
-    if (sub == 0 && r < a.R)
-      *reinterpret_cast<uint32_t*>(a.s_row + scale_offset(r, static_cast<uint64_t>(c0 / 16), a.kpad_row)) = word;
-    if (a.gdec_row != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && t == 0) *a.gdec_row = __fdiv_rn(1.0f, senc);
   }
-  if (a.q_col != nullptr) {
-    const bool rht = (a.flags & TE_NVFP4_RHT_COL) != 0;
-    const float senc = nv_senc(rht ? *a.amax_rht : *a.amax);
-    const int64_t c = c0 + lane_row, r = r0 + seg;
-    const bool valid = c < a.C && r < a.R;
-    float v[16];
+  if (do_col && p.live) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = tile[seg + i][lane_row];
-    if (rht) rht16(v, a.signs);
-    float bm = 0.0f;
-    if (two_d) {
-      bm = amax2d[sub][lane_row >> 4];
-    } else {
+    for (int i = 0; i < PC; ++i) {
+      float v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
+      for (int r = 0; r < 16; ++r) v[r] = p.at(r, i);
+      if (rht) rht16(v, a.signs);
+      float m = tile_max;
+      if (!two_d) {
+        m = 0.0f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(v[r]));
+      }
+      const uint32_t sc = nv_scale_code(m, senc_c);
+      const float rr = rtab[1][sc];
+      uint32_t lo = 0, hi = 0;
+      if (!SR) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) lo |= cvt_e2m1x2(__fmul_rn(v[2 * j], rr), __fmul_rn(v[2 * j + 1], rr)) << (8 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], rr), __fmul_rn(v[8 + 2 * j + 1], rr)) << (8 * j);
+      } else {
+        const uint64_t g = static_cast<uint64_t>(p.c0 + i) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(p.r0);
+        const uint4 r0 = nv_rand8(a, g >> 3, 1u);
+        const uint4 r1 = nv_rand8(a, (g >> 3) + 1, 1u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], rr), rand16_of(r0, k)) << (4 * k);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], rr), rand16_of(r1, k)) << (4 * k);
+      }
+      *reinterpret_cast<uint2*>(a.q_col + (p.c0 + i) * (a.R / 2) + p.r0 / 2) = make_uint2(lo, hi);
+      a.s_col[scale_offset(p.c0 + i, p.r0 / 16, a.kpad_col)] = static_cast<uint8_t>(sc);
     }
-    const uint64_t g0 = static_cast<uint64_t>(c) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(r);
-    const uint32_t sc = nv_quantize_block(v, bm, senc, sr, a, 1u, g0,
-                                          reinterpret_cast<uint2*>(a.q_col + c * (a.R / 2) + r / 2), valid);
-    uint32_t word = sc;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 1) << 8;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 2) << 16;
-    word |= __shfl_down_sync(0xFFFFFFFFu, sc, 3) << 24;
-    if (sub == 0 && c < a.C)
-      *reinterpret_cast<uint32_t*>(a.s_col + scale_offset(c, static_cast<uint64_t>(r0 / 16), a.kpad_col)) = word;
-    if (a.gdec_col != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && t == 0) *a.gdec_col = __fdiv_rn(1.0f, senc);
   }
 }
 
@@ -513,6 +561,9 @@ inline te_status check_2d(const void* x, te_dtype in, int64_t rows, int64_t cols
   if (!in_dtype_ok(in)) return TE_ERR_DTYPE;
   if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return TE_ERR_SHAPE;
   if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return TE_ERR_SHAPE;
+  // patches are counted with 64-bit indices; keep the grid within 2^31 blocks and
+  // element indices of the stochastic-rounding counters below 2^34
+  if (rows * cols >= (int64_t(1) << 34)) return TE_ERR_SHAPE;
   if (rows * cols > 0) {
     if (x == nullptr) return TE_ERR_NULL;
     if (!aligned16(x)) return TE_ERR_ALIGN;
@@ -520,27 +571,20 @@ inline te_status check_2d(const void* x, te_dtype in, int64_t rows, int64_t cols
   return TE_OK;
 }
 
-inline dim3 tile_grid(int64_t rows, int64_t cols) {
-  return dim3(static_cast<unsigned>((cols + kTile - 1) / kTile), static_cast<unsigned>((rows + kTile - 1) / kTile));
-}
-
-inline bool grid_ok(int64_t rows) { return (rows + kTile - 1) / kTile <= 65535; }
-
 te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, float* amax, float* amax_rht,
                       uint32_t signs, cudaStream_t st) {
   if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return record_cuda(cudaGetLastError());
   if (amax_rht != nullptr && cudaMemsetAsync(amax_rht, 0, sizeof(float), st) != cudaSuccess)
     return record_cuda(cudaGetLastError());
   if (rows * cols == 0) return TE_OK;
-  const int64_t items = (rows / 16) * (cols / 8);
-  const int64_t want = (items + kThreads - 1) / kThreads;
-  const unsigned blocks = static_cast<unsigned>(want < 1 ? 1 : (want > 65535 * 8 ? 65535 * 8 : want));
   if (in == TE_BF16) {
     const auto* p = static_cast<const __nv_bfloat16*>(x);
+    const unsigned blocks = patch_blocks(rows, cols, 16, 8);
     if (amax_rht) amax_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
     else amax_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, nullptr, signs);
   } else {
     const auto* p = static_cast<const float*>(x);
+    const unsigned blocks = patch_blocks(rows, cols, 16, 4);
     if (amax_rht) amax_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
     else amax_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, nullptr, signs);
   }
@@ -560,6 +604,8 @@ inline int64_t kpad_of(te_dtype fmt, int64_t cols) {
   return fmt == TE_E8M0 ? ((cols / 32 + 3) / 4) * 4 : ((cols / 16 + 15) / 16) * 16;
 }
 
+inline int vec_elems(te_dtype in, int bytes) { return bytes / (in == TE_BF16 ? 2 : 4); }
+
 }  // namespace
 }  // namespace te
 
@@ -572,7 +618,7 @@ te_status te_amax_reduce(const void* x, te_dtype in_dtype, int64_t rows, int64_t
   te_status s = check_2d(x, in_dtype, rows, cols);
   if (s != TE_OK) return s;
   if (amax == nullptr) return TE_ERR_NULL;
-  return launch_amax(x, in_dtype, rows, cols, amax, amax_rht, rht_signs, static_cast<cudaStream_t>(stream));
+  return launch_amax(x, in_dtype, rows, cols, amax, amax_rht, rht_signs & 0xFFFFu, static_cast<cudaStream_t>(stream));
 }
 
 te_status te_scale_update(const te_recipe* recipe, int is_backward, int n_tensors, float* hist, const float* amax,
@@ -607,7 +653,6 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
   if (compute_scale != 0 && compute_scale != 1) return TE_ERR_ARG;
   if (compute_scale ? amax_out == nullptr : scale == nullptr) return TE_ERR_NULL;
   if ((q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col))) return TE_ERR_ALIGN;
-  if (!grid_ok(rows)) return TE_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (compute_scale) {
     s = launch_amax(x, in_dtype, rows, cols, amax_out, nullptr, 0, st);
@@ -616,18 +661,18 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return record_cuda(cudaGetLastError());
   }
   if (rows * cols == 0 && scale_inv_out == nullptr) return TE_OK;
-  // An empty tensor still launches one (load-free) tile so that scale_inv_out is published.
+  // An empty tensor still launches one (load-free) block so that scale_inv_out is published.
   Fp8Args a{rows, cols, scale, amax_out, compute_scale, fmt == TE_E4M3 ? 448.0f : 57344.0f, q_row, q_col,
             compute_scale ? nullptr : amax_out, scale_inv_out};
-  const dim3 grid = rows * cols == 0 ? dim3(1, 1) : tile_grid(rows, cols);
+  const unsigned blocks = patch_blocks(rows, cols, 16, vec_elems(in_dtype, 16));
   if (in_dtype == TE_BF16) {
     const auto* p = static_cast<const __nv_bfloat16*>(x);
-    if (fmt == TE_E4M3) fp8_kernel<__nv_bfloat16, false><<<grid, kThreads, 0, st>>>(p, a);
-    else fp8_kernel<__nv_bfloat16, true><<<grid, kThreads, 0, st>>>(p, a);
+    if (fmt == TE_E4M3) fp8_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, a);
+    else fp8_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, a);
   } else {
     const auto* p = static_cast<const float*>(x);
-    if (fmt == TE_E4M3) fp8_kernel<float, false><<<grid, kThreads, 0, st>>>(p, a);
-    else fp8_kernel<float, true><<<grid, kThreads, 0, st>>>(p, a);
+    if (fmt == TE_E4M3) fp8_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, a);
+    else fp8_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, a);
   }
   count_launch();
   return launch_status();
@@ -641,15 +686,21 @@ te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int6
   if ((q_row && cols % 32) || (q_col && rows % 32)) return TE_ERR_SHAPE;
   if ((q_row && (!aligned16(q_row) || !aligned16(s_row))) || (q_col && (!aligned16(q_col) || !aligned16(s_col))))
     return TE_ERR_ALIGN;
-  if (!grid_ok(rows)) return TE_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (q_row && (s = zero_scales(s_row, TE_E8M0, rows, cols, st)) != TE_OK) return s;
   if (q_col && (s = zero_scales(s_col, TE_E8M0, cols, rows, st)) != TE_OK) return s;
   if (rows * cols == 0 || (!q_row && !q_col)) return TE_OK;
   MxArgs a{rows, cols, q_row, s_row, kpad_of(TE_E8M0, cols), q_col, s_col, kpad_of(TE_E8M0, rows)};
-  const dim3 grid = tile_grid(rows, cols);
-  if (in_dtype == TE_BF16) mxfp8_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
-  else mxfp8_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), a);
+  const int pc = vec_elems(in_dtype, 8);
+  if (q_col) {
+    const unsigned blocks = patch_blocks(rows, cols, 32, pc);
+    if (in_dtype == TE_BF16) mxfp8_kernel<__nv_bfloat16, 32><<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
+    else mxfp8_kernel<float, 32><<<blocks, kThreads, 0, st>>>(static_cast<const float*>(x), a);
+  } else {
+    const unsigned blocks = patch_blocks(rows, cols, 16, pc);
+    if (in_dtype == TE_BF16) mxfp8_kernel<__nv_bfloat16, 16><<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
+    else mxfp8_kernel<float, 16><<<blocks, kThreads, 0, st>>>(static_cast<const float*>(x), a);
+  }
   count_launch();
   return launch_status();
 }
@@ -669,19 +720,27 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   if (col && (flags & TE_NVFP4_RHT_COL) && amax_rht == nullptr) return TE_ERR_NULL;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) || (col && (!aligned16(q_col) || !aligned16(s_col))))
     return TE_ERR_ALIGN;
-  if (rows * cols >= (int64_t(1) << 34) || !grid_ok(rows)) return TE_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (row && (s = zero_scales(s_row, TE_UE4M3, rows, cols, st)) != TE_OK) return s;
   if (col && (s = zero_scales(s_col, TE_UE4M3, cols, rows, st)) != TE_OK) return s;
-  if (rows * cols == 0 || (!row && !col)) return TE_OK;
+  if (!row && !col) return TE_OK;
+  // An empty tensor launches one load-free block that publishes the S_dec outputs.
   NvArgs a{rows, cols, flags, rht_signs & 0xFFFFu,
            static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
            static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
            amax, amax_rht, q_row, s_row, gdec_row, kpad_of(TE_UE4M3, cols),
            q_col, s_col, gdec_col, kpad_of(TE_UE4M3, rows)};
-  const dim3 grid = tile_grid(rows, cols);
-  if (in_dtype == TE_BF16) nvfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
-  else nvfp4_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), a);
+  const bool sr = (flags & TE_NVFP4_SR) != 0;
+  const unsigned blocks = patch_blocks(rows, cols, 16, vec_elems(in_dtype, 16));
+  if (in_dtype == TE_BF16) {
+    const auto* p = static_cast<const __nv_bfloat16*>(x);
+    if (sr) nvfp4_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, a);
+    else nvfp4_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, a);
+  } else {
+    const auto* p = static_cast<const float*>(x);
+    if (sr) nvfp4_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, a);
+    else nvfp4_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, a);
+  }
   count_launch();
   return launch_status();
 }
