@@ -75,24 +75,28 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Stochastic rounding of v to E2M1: the magnitude moves up to the next grid
-// point iff r16 * 2^-16 < (|v| - lo) / (hi - lo); |v| >= 6 saturates.
+// Stochastic rounding of v to E2M1, branch-free: the magnitude moves up to the
+// next E2M1 value iff r16 * 2^-16 < (|v| - lo) / (hi - lo); |v| >= 6 saturates.
+// With a = |v| = 2^e (1 + M 2^-23), the fraction is exact in integers:
+//   a >= 1       : lo keeps the top mantissa bit, frac = (M mod 2^22) / 2^22
+//   a in [0.5, 1): lo = 0.5, frac = M / 2^23
+//   a < 0.5      : lo = 0, frac = 2a, compared as r16 < a * 2^17 (both exact in fp32)
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-  const float a = fabsf(v);
-  const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-  if (a >= 6.0f) return sign | 7u;
-  float lo, inv_span;
-  uint32_t code;
-  if (a < 0.5f) { lo = 0.0f; inv_span = 2.0f; code = 0; }
-  else if (a < 1.0f) { lo = 0.5f; inv_span = 2.0f; code = 1; }
-  else if (a < 1.5f) { lo = 1.0f; inv_span = 2.0f; code = 2; }
-  else if (a < 2.0f) { lo = 1.5f; inv_span = 2.0f; code = 3; }
-  else if (a < 3.0f) { lo = 2.0f; inv_span = 1.0f; code = 4; }
-  else if (a < 4.0f) { lo = 3.0f; inv_span = 1.0f; code = 5; }
-  else { lo = 4.0f; inv_span = 0.5f; code = 6; }
-  const float frac = __fmul_rn(__fsub_rn(a, lo), inv_span);  // exact
-  const float thr = __fmul_rn(static_cast<float>(r16), 1.52587890625e-5f);  // exact: r16 * 2^-16
-  return sign | (thr < frac ? code + 1u : code);
+  const uint32_t bits = __float_as_uint(v);
+  const uint32_t u = bits & 0x7FFFFFFFu;
+  const uint32_t sign = (bits >> 28) & 8u;
+  const uint32_t ef = u >> 23;
+  const bool ge1 = ef >= 127u;
+  const bool half = ef == 126u;
+  const uint32_t D = ge1 ? (u & 0x3FFFFFu) : (u & 0x7FFFFFu);
+  const uint32_t Rs = ge1 ? (r16 << 6) : (r16 << 7);
+  const bool up_frac = Rs < D;
+  const bool up_small = __uint2float_rn(r16) < __fmul_rn(__uint_as_float(u), 131072.0f);
+  const uint32_t lo_code = ge1 ? (((ef - 126u) << 1) | ((u >> 22) & 1u)) : (half ? 1u : 0u);
+  const bool up = (ge1 || half) ? up_frac : up_small;
+  uint32_t code = lo_code + (up ? 1u : 0u);
+  code = (u >= 0x40C00000u) ? 7u : code;  // |v| >= 6
+  return sign | code;
 }
 
 // ---- 16-point random Hadamard transform ----------------------------------------------------
@@ -287,65 +291,7 @@ __device__ __forceinline__ float current_scale(float a, float fmax) {
   return isfinite(s) ? s : 1.0f;
 }
 
-// ---- FP8 ----------------------------------------------------------------------------------------
-struct Fp8Args {
-  int64_t R, C;
-  const float* scale;     // Delayed: the scale to use
-  const float* amax_in;   // Current: the tensor amax
-  int current;
-  float fmax;
-  uint8_t* q_row;
-  uint8_t* q_col;
-  float* amax_out;        // Delayed: fused amax (nullable)
-  float* scale_inv_out;   // nullable
-};
-
-template <bool E5M2>
-__device__ __forceinline__ uint32_t fp8x2(float a, float b) {
-  return E5M2 ? cvt_e5m2x2(a, b) : cvt_e4m3x2(a, b);
-}
-
-template <typename T, bool E5M2>
-__global__ void __launch_bounds__(kThreads, 2) fp8_kernel(const T* __restrict__ x, Fp8Args a) {
-  using P = Patch<T, 16, 16>;
-  constexpr int PC = P::PC;
-  P p;
-  p.load(x, a.R, a.C);
-  const float s = a.current ? current_scale(*a.amax_in, a.fmax) : *a.scale;
-  if (p.live && a.q_row != nullptr) {
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      uint32_t w[PC / 4];
-#pragma unroll
-      for (int j = 0; j < PC / 4; ++j) {
-        const uint32_t lo = fp8x2<E5M2>(__fmul_rn(p.at(r, 4 * j), s), __fmul_rn(p.at(r, 4 * j + 1), s));
-        const uint32_t hi = fp8x2<E5M2>(__fmul_rn(p.at(r, 4 * j + 2), s), __fmul_rn(p.at(r, 4 * j + 3), s));
-        w[j] = lo | (hi << 16);
-      }
-      uint8_t* dst = a.q_row + (p.r0 + r) * a.C + p.c0;
-      if (PC == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[PC / 4 - 1]);
-      else *reinterpret_cast<uint32_t*>(dst) = w[0];
-    }
-  }
-  if (p.live && a.q_col != nullptr) {
-#pragma unroll
-    for (int i = 0; i < PC; ++i) {
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = fp8x2<E5M2>(__fmul_rn(p.at(4 * j, i), s), __fmul_rn(p.at(4 * j + 1, i), s));
-        const uint32_t hi = fp8x2<E5M2>(__fmul_rn(p.at(4 * j + 2, i), s), __fmul_rn(p.at(4 * j + 3, i), s));
-        w[j] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint4*>(a.q_col + (p.c0 + i) * a.R + p.r0) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-  if (a.scale_inv_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.scale_inv_out = __fdiv_rn(1.0f, s);
-  if (a.amax_out != nullptr) block_max_to(p.absmax(), a.amax_out);
-}
-
-// ---- MXFP8 ----------------------------------------------------------------------------------------
-// Shared exponent of a block: clamp(floor(log2 amax) - 8, -127, 127); -127 for a zero block.
+// Shared exponent of an MXFP8 block: clamp(floor(log2 amax) - 8, -127, 127); -127 for a zero block.
 __device__ __forceinline__ int mx_exponent(float amax) {
   const uint32_t b = __float_as_uint(amax);
   if (b == 0) return -127;
@@ -356,200 +302,375 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 }
 __device__ __forceinline__ float mx_mult(int E) { return __uint_as_float(static_cast<uint32_t>(127 - E) << 23); }
 
-struct MxArgs {
-  int64_t R, C;
-  uint8_t* q_row;
-  uint8_t* s_row;
-  int64_t kpad_row;  // padded scale columns of the row copy
-  uint8_t* q_col;
-  uint8_t* s_col;
-  int64_t kpad_col;
-};
-
-// PR = 32 when the col copy is requested (one column block per patch), else 16.
-template <typename T, int PR>
-__global__ void __launch_bounds__(kThreads, 2) mxfp8_kernel(const T* __restrict__ x, MxArgs a) {
-  using P = Patch<T, 8, PR>;
-  constexpr int PC = P::PC;
-  constexpr int LANES = 32 / PC;  // threads sharing one row block of 32
-  P p;
-  p.load(x, a.R, a.C);
-  if (a.q_row != nullptr) {
-    const bool first = ((p.c0 / PC) % LANES) == 0;
-#pragma unroll
-    for (int r = 0; r < PR; ++r) {
-      float m = 0.0f;
-#pragma unroll
-      for (int i = 0; i < PC; ++i) m = fmaxf(m, fabsf(p.at(r, i)));
-      m = group_max<LANES>(m);
-      const int E = mx_exponent(m);
-      const float mult = mx_mult(E);
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < PC / 2; ++j)
-        w |= cvt_e4m3x2(__fmul_rn(p.at(r, 2 * j), mult), __fmul_rn(p.at(r, 2 * j + 1), mult)) << (16 * j);
-      if (p.live) {
-        uint8_t* dst = a.q_row + (p.r0 + r) * a.C + p.c0;
-        if (PC == 4) *reinterpret_cast<uint32_t*>(dst) = w;
-        else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
-        if (first) a.s_row[scale_offset(p.r0 + r, p.c0 / 32, a.kpad_row)] = static_cast<uint8_t>(E + 127);
-      }
-    }
-  }
-  if (PR == 32 && a.q_col != nullptr && p.live) {
-#pragma unroll
-    for (int i = 0; i < PC; ++i) {
-      float m = 0.0f;
-#pragma unroll
-      for (int r = 0; r < PR; ++r) m = fmaxf(m, fabsf(p.at(r, i)));
-      const int E = mx_exponent(m);
-      const float mult = mx_mult(E);
-      uint32_t w[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(p.at(4 * j, i), mult), __fmul_rn(p.at(4 * j + 1, i), mult));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(p.at(4 * j + 2, i), mult), __fmul_rn(p.at(4 * j + 3, i), mult));
-        w[j] = lo | (hi << 16);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(a.q_col + (p.c0 + i) * a.R + p.r0);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      a.s_col[scale_offset(p.c0 + i, p.r0 / 32, a.kpad_col)] = static_cast<uint8_t>(E + 127);
-    }
-  }
-}
-
-// ---- NVFP4 ----------------------------------------------------------------------------------------
-struct NvArgs {
-  int64_t R, C;
-  uint32_t flags, signs;
-  uint32_t seed_lo, seed_hi, off_lo, off_hi;
-  const float* amax;
-  const float* amax_rht;
-  uint8_t* q_row;
-  uint8_t* s_row;
-  float* gdec_row;
-  int64_t kpad_row;
-  uint8_t* q_col;
-  uint8_t* s_col;
-  float* gdec_col;
-  int64_t kpad_col;
-};
-
 __device__ __forceinline__ float nv_senc(float A) {
   if (!(A > 0.0f)) return 1.0f;
   const float s = __fdiv_rn(2688.0f, A);
   return isfinite(s) ? s : 1.0f;
 }
-
 // UE4M3 block-scale code of a block with amax bm: RN(fl32(fl32(bm / 6) * S_enc)).
 __device__ __forceinline__ uint32_t nv_scale_code(float bm, float senc) {
   return cvt_e4m3x2(__fmul_rn(__fdiv_rn(bm, 6.0f), senc), 0.0f) & 0x7Fu;
 }
-
-// The 16-bit random values of the 8 elements g8*8 .. g8*8+7 of a copy (element
-// 2k + h takes half h of word k of Philox(counter = (g8, copy, offset))).
-__device__ __forceinline__ uint4 nv_rand8(const NvArgs& a, uint64_t g8, uint32_t copy_id) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(g8), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
-}
-__device__ __forceinline__ uint32_t rand16_of(const uint4& w, int k) {  // k = element index within the 8
-  const uint32_t word = raw_word(w, k >> 1);
+__device__ __forceinline__ uint32_t rand16_of(const uint4& w, int k) {  // k-th of the 8 values of one output
+  const uint32_t word = k < 2 ? w.x : (k < 4 ? w.y : (k < 6 ? w.z : w.w));
   return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
-template <typename T, bool SR>
-__global__ void __launch_bounds__(kThreads, 2) nvfp4_kernel(const T* __restrict__ x, NvArgs a) {
-  using P = Patch<T, 16, 16>;
-  constexpr int PC = P::PC;
-  constexpr int LANES = 16 / PC;  // threads sharing one row block of 16
-  __shared__ float rtab[2][128];  // r = fl32(S_enc / dec(code)) for the row / col copy
-  const bool do_row = a.q_row != nullptr, do_col = a.q_col != nullptr;
-  const bool two_d = (a.flags & TE_NVFP4_2D) != 0, rht = (a.flags & TE_NVFP4_RHT_COL) != 0;
-  const float senc_r = do_row ? nv_senc(*a.amax) : 1.0f;
-  const float senc_c = do_col ? nv_senc(rht ? *a.amax_rht : *a.amax) : 1.0f;
-  if (threadIdx.x < 128) {
-    const float dv = ue4m3_value(threadIdx.x);
-    rtab[0][threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_r, dv) : 0.0f;
-    rtab[1][threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_c, dv) : 0.0f;
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (do_row && a.gdec_row != nullptr) *a.gdec_row = __fdiv_rn(1.0f, senc_r);
-    if (do_col && a.gdec_col != nullptr) *a.gdec_col = __fdiv_rn(1.0f, senc_c);
-  }
-  P p;
-  p.load(x, a.R, a.C);
-  __syncthreads();
-  float tile_max = 0.0f;  // 2D: amax of the 16 x 16 tile this patch belongs to
-  if (two_d) tile_max = group_max<LANES>(p.absmax());
+// ---- warp-tile quantizers (FP8, MXFP8, NVFP4) ------------------------------------------------------
+// Persistent CTAs of 8 warps; every warp owns a private 3-stage ring of 64-row x
+// 128-byte tiles (64 x 64 bf16 or 64 x 32 fp32) that its lane 0 fills with TMA
+// (128-byte swizzle), so warps never wait on each other.  Per tile, the row copy
+// is produced by lane l from tile rows l and l + 32 (16-byte shared loads whose
+// swizzled chunks are distinct across each 8-lane phase) and the col copy by lane
+// l from its 4-byte column slice (32 distinct banks per row); each lane then writes
+// whole 64-row / 64-column runs of the copies.  All of a warp's stores of one tile
+// are 16-byte aligned vectors.
 
-  if (do_row) {
-    const bool first = ((p.c0 / PC) % LANES) == 0;
+enum QFmt { kQE4M3 = 0, kQE5M2 = 1, kQMX = 2, kQNV = 3 };
+
+struct TileArgs {
+  int64_t R, C;
+  uint8_t* q_row;
+  uint8_t* q_col;
+  // per-tensor FP8
+  const float* scale;
+  const float* amax_in;
+  int current;
+  float fmax;
+  float* amax_out;
+  float* scale_inv_out;
+  // block scales (MXFP8 / NVFP4)
+  uint8_t* s_row;
+  uint8_t* s_col;
+  int64_t kpad_row, kpad_col;
+  // NVFP4
+  uint32_t flags, signs, seed_lo, seed_hi, off_lo, off_hi;
+  const float* amax;
+  const float* amax_rht;
+  float* gdec_row;
+  float* gdec_col;
+  int* err;
+};
+
+constexpr int kQWarps = 8;
+constexpr int kQStages = 3;
+constexpr int kQTileBytes = 64 * 128;
+constexpr int kQSmem = kQWarps * kQStages * kQTileBytes + kQWarps * kQStages * 8 + 1024 + 1024;
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte chunk j of tile row r (128-byte swizzle: chunk j of row r sits at j ^ (r % 8)).
+__device__ __forceinline__ uint4 tile_chunk(const uint8_t* tile, int r, int j) {
+  return *reinterpret_cast<const uint4*>(tile + r * 128 + ((j ^ (r & 7)) << 4));
+}
+// 4-byte word w (0..31) of tile row r.
+__device__ __forceinline__ uint32_t tile_word(const uint8_t* tile, int r, int w) {
+  return *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((w >> 2) ^ (r & 7)) << 4) + ((w & 3) << 2));
+}
+
+// 16 consecutive bf16 elements from two 16-byte chunks (c0 holds 0..7, c1 8..15).
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& c0, const uint4& c1, float (&v)[16], int) {
+  {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float m = 0.0f;
-      if (!two_d) {
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ uint4 fp8_pack16(const float (&v)[16], float s) {
+  uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < PC; ++i) m = fmaxf(m, fabsf(p.at(r, i)));
-        m = group_max<LANES>(m);
-      } else {
-        m = tile_max;
+  for (int j = 0; j < 4; ++j) {
+    const float a0 = __fmul_rn(v[4 * j], s), a1 = __fmul_rn(v[4 * j + 1], s);
+    const float a2 = __fmul_rn(v[4 * j + 2], s), a3 = __fmul_rn(v[4 * j + 3], s);
+    const uint32_t lo = FMT == kQE5M2 ? cvt_e5m2x2(a0, a1) : cvt_e4m3x2(a0, a1);
+    const uint32_t hi = FMT == kQE5M2 ? cvt_e5m2x2(a2, a3) : cvt_e4m3x2(a2, a3);
+    w[j] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// NVFP4 block of 16 values (block amax bm given): returns 8 packed bytes; *code = scale code.
+template <bool SR>
+__device__ __forceinline__ uint2 nv_block(const float (&v)[16], float bm, float senc, const float* rtab,
+                                          const TileArgs& a, uint64_t g0, uint32_t copy_id, uint32_t* code) {
+  const uint32_t sc = nv_scale_code(bm, senc);
+  *code = sc;
+  const float r = rtab[sc];
+  uint32_t lo = 0, hi = 0;
+  if (!SR) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) lo |= cvt_e2m1x2(__fmul_rn(v[2 * j], r), __fmul_rn(v[2 * j + 1], r)) << (8 * j);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], r), __fmul_rn(v[9 + 2 * j], r)) << (8 * j);
+  } else {
+    const uint4 w0 = philox4x32_10(make_uint4(static_cast<uint32_t>(g0 >> 3), copy_id, a.off_lo, a.off_hi),
+                                   a.seed_lo, a.seed_hi);
+    const uint4 w1 = philox4x32_10(make_uint4(static_cast<uint32_t>(g0 >> 3) + 1u, copy_id, a.off_lo, a.off_hi),
+                                   a.seed_lo, a.seed_hi);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], r), rand16_of(w0, k)) << (4 * k);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], r), rand16_of(w1, k)) << (4 * k);
+  }
+  return make_uint2(lo, hi);
+}
+
+template <int L>
+__device__ __forceinline__ float lanes_max(float v) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// One 64 x 64 bf16 tile.  (The 32-column fp32 tile uses the same code with half
+// of the lanes' column slices; see NCL / NB16.)
+template <typename T, int FMT, bool SR>
+__device__ __forceinline__ void quantize_tile(const uint8_t* tile, int64_t r0, int64_t c0, const TileArgs& a,
+                                              float s_fp8, float senc_r, float senc_c, const float* rtab_r,
+                                              const float* rtab_c, int lane, float& lmax) {
+  constexpr int TC = 128 / sizeof(T);   // tile columns
+  constexpr int NB16 = TC / 16;         // 16-column blocks per tile row
+  const bool two_d = FMT == kQNV && (a.flags & TE_NVFP4_2D) != 0;
+  const bool rht = FMT == kQNV && (a.flags & TE_NVFP4_RHT_COL) != 0;
+  const bool need_max = a.amax_out != nullptr;
+
+  // ---------------- row copy: lane handles tile rows lane and lane + 32
+  if (a.q_row != nullptr) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int rr = lane + 32 * h;
+      const int64_t row = r0 + rr;
+      float v[NB16][16];
+#pragma unroll
+      for (int j = 0; j < NB16; ++j) {
+        if constexpr (sizeof(T) == 2) {
+          unpack16<T>(tile_chunk(tile, rr, 2 * j), tile_chunk(tile, rr, 2 * j + 1), v[j], 0);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 c = tile_chunk(tile, rr, 4 * j + q);
+            v[j][4 * q] = __uint_as_float(c.x);
+            v[j][4 * q + 1] = __uint_as_float(c.y);
+            v[j][4 * q + 2] = __uint_as_float(c.z);
+            v[j][4 * q + 3] = __uint_as_float(c.w);
+          }
+        }
       }
-      const uint32_t sc = nv_scale_code(m, senc_r);
-      const float rr = rtab[0][sc];
-      const uint64_t g = static_cast<uint64_t>(p.r0 + r) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(p.c0);
-      uint32_t w = 0;
-      if (!SR) {
+      float bmax[NB16];
 #pragma unroll
-        for (int j = 0; j < PC / 2; ++j)
-          w |= cvt_e2m1x2(__fmul_rn(p.at(r, 2 * j), rr), __fmul_rn(p.at(r, 2 * j + 1), rr)) << (8 * j);
-      } else {
-        const uint4 rnd = nv_rand8(a, g >> 3, 0u);
-        const int k0 = static_cast<int>(g & 7);
+      for (int j = 0; j < NB16; ++j) {
+        float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < PC; ++i) w |= e2m1_sr(__fmul_rn(p.at(r, i), rr), rand16_of(rnd, k0 + i)) << (4 * i);
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[j][i]));
+        bmax[j] = m;
+        if (need_max) lmax = fmaxf(lmax, m);
       }
-      if (p.live) {
-        uint8_t* dst = a.q_row + (p.r0 + r) * (a.C / 2) + p.c0 / 2;
-        if (PC == 8) *reinterpret_cast<uint32_t*>(dst) = w;
-        else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
-        if (first) a.s_row[scale_offset(p.r0 + r, p.c0 / 16, a.kpad_row)] = static_cast<uint8_t>(sc);
+      if (two_d) {
+#pragma unroll
+        for (int j = 0; j < NB16; ++j) bmax[j] = lanes_max<16>(bmax[j]);  // 16 rows x 16 cols
+      }
+      const bool row_ok = row < a.R;
+      if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < NB16; ++j)
+            if (c0 + 16 * j < a.C)
+              *reinterpret_cast<uint4*>(a.q_row + row * a.C + c0 + 16 * j) = fp8_pack16<FMT>(v[j], s_fp8);
+        }
+      } else if constexpr (FMT == kQMX) {
+        // blocks of 32 = pairs of 16-blocks
+#pragma unroll
+        for (int j = 0; j < NB16; j += 2) {
+          const int E = mx_exponent(fmaxf(bmax[j], bmax[j + 1]));
+          const float mult = mx_mult(E);
+          if (row_ok && c0 + 16 * j < a.C) {
+            uint4* dst = reinterpret_cast<uint4*>(a.q_row + row * a.C + c0 + 16 * j);
+            dst[0] = fp8_pack16<kQE4M3>(v[j], mult);
+            dst[1] = fp8_pack16<kQE4M3>(v[j + 1], mult);
+            a.s_row[scale_offset(row, (c0 + 16 * j) / 32, a.kpad_row)] = static_cast<uint8_t>(E + 127);
+          }
+        }
+      } else {
+        uint32_t codes = 0;
+#pragma unroll
+        for (int j = 0; j < NB16; ++j) {
+          uint32_t sc;
+          const uint64_t g0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(c0 + 16 * j);
+          const uint2 q = nv_block<SR>(v[j], bmax[j], senc_r, rtab_r, a, g0, 0u, &sc);
+          codes |= sc << (8 * j);
+          if (row_ok && c0 + 16 * j < a.C)
+            *reinterpret_cast<uint2*>(a.q_row + row * (a.C / 2) + (c0 + 16 * j) / 2) = q;
+        }
+        if (row_ok) {
+          uint8_t* sdst = a.s_row + scale_offset(row, c0 / 16, a.kpad_row);
+          if (NB16 == 4) *reinterpret_cast<uint32_t*>(sdst) = codes;
+          else *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(codes);
+        }
       }
     }
   }
-  if (do_col && p.live) {
+
+  // ---------------- col copy: lane handles the 4-byte column slice `lane` (2 bf16 / 1 fp32 columns)
+  if (a.q_col != nullptr) {
+    constexpr int NCL = 4 / sizeof(T);
+    constexpr int RB = FMT == kQMX ? 32 : 16;   // rows per col-copy block
+#pragma unroll 1
+    for (int b = 0; b < 64 / RB; ++b) {
+      float v[NCL][RB];
 #pragma unroll
-    for (int i = 0; i < PC; ++i) {
-      float v[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) v[r] = p.at(r, i);
-      if (rht) rht16(v, a.signs);
-      float m = tile_max;
-      if (!two_d) {
-        m = 0.0f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(v[r]));
+      for (int r = 0; r < RB; ++r) {
+        const uint32_t w = tile_word(tile, b * RB + r, lane);
+        if constexpr (sizeof(T) == 2) {
+          v[0][r] = __uint_as_float(w << 16);
+          v[NCL - 1][r] = __uint_as_float(w & 0xFFFF0000u);
+        } else {
+          v[0][r] = __uint_as_float(w);
+        }
       }
-      const uint32_t sc = nv_scale_code(m, senc_c);
-      const float rr = rtab[1][sc];
-      uint32_t lo = 0, hi = 0;
-      if (!SR) {
+      const int64_t rb0 = r0 + b * RB;
+      const bool rows_ok = rb0 < a.R;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= cvt_e2m1x2(__fmul_rn(v[2 * j], rr), __fmul_rn(v[2 * j + 1], rr)) << (8 * j);
+      for (int q = 0; q < NCL; ++q) {
+        const int64_t col = c0 + lane * NCL + q;
+        const bool ok = rows_ok && col < a.C;
+        if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
+          if (need_max && a.q_row == nullptr)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], rr), __fmul_rn(v[8 + 2 * j + 1], rr)) << (8 * j);
-      } else {
-        const uint64_t g = static_cast<uint64_t>(p.c0 + i) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(p.r0);
-        const uint4 r0 = nv_rand8(a, g >> 3, 1u);
-        const uint4 r1 = nv_rand8(a, (g >> 3) + 1, 1u);
+            for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
+          if (ok) *reinterpret_cast<uint4*>(a.q_col + col * a.R + rb0) = fp8_pack16<FMT>(v[q], s_fp8);
+        } else if constexpr (FMT == kQMX) {
+          float m = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], rr), rand16_of(r0, k)) << (4 * k);
+          for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
+          const int E = mx_exponent(m);
+          const float mult = mx_mult(E);
+          if (ok) {
+            float h0[16], h1[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], rr), rand16_of(r1, k)) << (4 * k);
+            for (int r = 0; r < 16; ++r) h0[r] = v[q][r], h1[r] = v[q][16 + r];
+            uint4* dst = reinterpret_cast<uint4*>(a.q_col + col * a.R + rb0);
+            dst[0] = fp8_pack16<kQE4M3>(h0, mult);
+            dst[1] = fp8_pack16<kQE4M3>(h1, mult);
+            a.s_col[scale_offset(col, rb0 / 32, a.kpad_col)] = static_cast<uint8_t>(E + 127);
+          }
+        } else {
+          float x[16];
+#pragma unroll
+          for (int r = 0; r < 16; ++r) x[r] = v[q][r];
+          if (rht) rht16(x, a.signs);
+          float m = 0.0f;
+#pragma unroll
+          for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(x[r]));
+          if (two_d) {
+            // 16 x 16 tile amax: the tile's 16 columns are spread over 16 / NCL lanes
+            float m2 = 0.0f;
+#pragma unroll
+            for (int qq = 0; qq < NCL; ++qq)
+#pragma unroll
+              for (int r = 0; r < 16; ++r) m2 = fmaxf(m2, fabsf(v[qq][r]));
+            m = lanes_max<16 / NCL>(m2);
+          }
+          uint32_t sc;
+          const uint64_t g0 = static_cast<uint64_t>(col) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(rb0);
+          const uint2 qv = nv_block<SR>(x, m, senc_c, rtab_c, a, g0, 1u, &sc);
+          if (ok) {
+            *reinterpret_cast<uint2*>(a.q_col + col * (a.R / 2) + rb0 / 2) = qv;
+            a.s_col[scale_offset(col, rb0 / 16, a.kpad_col)] = static_cast<uint8_t>(sc);
+          }
+        }
       }
-      *reinterpret_cast<uint2*>(a.q_col + (p.c0 + i) * (a.R / 2) + p.r0 / 2) = make_uint2(lo, hi);
-      a.s_col[scale_offset(p.c0 + i, p.r0 / 16, a.kpad_col)] = static_cast<uint8_t>(sc);
     }
+  }
+}
+
+template <typename T, int FMT, bool SR>
+__global__ void __launch_bounds__(kQWarps * 32, 1)
+    qtile_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ TileArgs a) {
+  constexpr int TC = 128 / sizeof(T);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = dev::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + warp * kQStages * kQTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQWarps * kQStages * kQTileBytes) + warp * kQStages;
+  float* rtab = reinterpret_cast<float*>(smem + kQWarps * kQStages * kQTileBytes + kQWarps * kQStages * 8);
+
+  float s_fp8 = 1.0f, senc_r = 1.0f, senc_c = 1.0f;
+  if (FMT == kQE4M3 || FMT == kQE5M2) s_fp8 = a.current ? current_scale(*a.amax_in, a.fmax) : *a.scale;
+  if (FMT == kQNV) {
+    const bool rht = (a.flags & TE_NVFP4_RHT_COL) != 0;
+    if (a.q_row != nullptr) senc_r = nv_senc(*a.amax);
+    if (a.q_col != nullptr) senc_c = nv_senc(rht ? *a.amax_rht : *a.amax);
+    if (threadIdx.x < 128) {
+      const float dv = ue4m3_value(threadIdx.x);
+      rtab[threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_r, dv) : 0.0f;
+      rtab[128 + threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_c, dv) : 0.0f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (a.gdec_row != nullptr) *a.gdec_row = __fdiv_rn(1.0f, senc_r);
+      if (a.gdec_col != nullptr) *a.gdec_col = __fdiv_rn(1.0f, senc_c);
+    }
+  }
+  if ((FMT == kQE4M3 || FMT == kQE5M2) && a.scale_inv_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *a.scale_inv_out = __fdiv_rn(1.0f, s_fp8);
+  if (lane == 0) {
+    for (int s = 0; s < kQStages; ++s) dev::mbar_init(&bars[s], 1);
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int64_t tiles_c = (a.C + TC - 1) / TC;
+  const int64_t n = ((a.R + 63) / 64) * tiles_c;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * kQWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kQWarps + warp;
+  if (lane == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      const int64_t t = first + s * W;
+      if (t < n) {
+        dev::mbar_expect_tx(&bars[s], kQTileBytes);
+        dev::tma_load_2d(ring + s * kQTileBytes, &tm, &bars[s], static_cast<int>((t % tiles_c) * 128),
+                         static_cast<int>((t / tiles_c) * 64));
+      }
+    }
+  }
+  int abort_flag = 0;
+  float lmax = 0.0f;
+  int k = 0;
+  for (int64_t t = first; t < n; t += W, ++k) {
+    const int s = k % kQStages;
+    const uint32_t ph = static_cast<uint32_t>(k / kQStages) & 1u;
+    if (!dev::mbar_wait(&bars[s], ph, &abort_flag, a.err)) break;
+    quantize_tile<T, FMT, SR>(ring + s * kQTileBytes, (t / tiles_c) * 64, (t % tiles_c) * TC, a, s_fp8, senc_r,
+                              senc_c, rtab, rtab + 128, lane, lmax);
+    __syncwarp();
+    fence_proxy_async_smem();
+    const int64_t nt = t + kQStages * W;
+    if (lane == 0 && nt < n) {
+      dev::mbar_expect_tx(&bars[s], kQTileBytes);
+      dev::tma_load_2d(ring + s * kQTileBytes, &tm, &bars[s], static_cast<int>((nt % tiles_c) * 128),
+                       static_cast<int>((nt / tiles_c) * 64));
+    }
+  }
+  if (abort_flag) {
+    // bounded wait for this warp's own copies still in flight before the CTA exits
+    int dummy = 0;
+    for (int j = 0; j < kQStages; ++j) {
+      const int kk = k + j;
+      const int64_t t = first + static_cast<int64_t>(kk) * W;
+      if (t < n) dev::mbar_wait(&bars[kk % kQStages], static_cast<uint32_t>(kk / kQStages) & 1u, &dummy, a.err);
+    }
+  }
+  if ((FMT == kQE4M3 || FMT == kQE5M2) && a.amax_out != nullptr) {
+    lmax = warp_max(lmax);
+    if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(a.amax_out), __float_as_uint(lmax));
   }
 }
 
@@ -604,7 +725,41 @@ inline int64_t kpad_of(te_dtype fmt, int64_t cols) {
   return fmt == TE_E8M0 ? ((cols / 32 + 3) / 4) * 4 : ((cols / 16 + 15) / 16) * 16;
 }
 
-inline int vec_elems(te_dtype in, int bytes) { return bytes / (in == TE_BF16 ? 2 : 4); }
+
+template <typename T, int FMT, bool SR>
+te_status launch_qtile(const void* x, int64_t R, int64_t C, TileArgs a, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
+    if (cudaFuncSetAttribute(qtile_kernel<T, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+        cudaSuccess)
+      return record_cuda(cudaGetLastError());
+    attr_set[dev_id] = true;
+  }
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof(tm));
+  if (R * C > 0) {
+    te_status s = make_tmap_2d(&tm, x, static_cast<uint64_t>(C) * sizeof(T), static_cast<uint64_t>(R), 64);
+    if (s != TE_OK) return s;
+  }
+  a.err = device_error_word();
+  if (a.err == nullptr) return record_cuda(cudaErrorInvalidDevice);
+  constexpr int TC = 128 / sizeof(T);
+  const int64_t tiles = ((R + 63) / 64) * ((C + TC - 1) / TC);
+  int64_t grid = (tiles + kQWarps - 1) / kQWarps;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), kQWarps * 32, kQSmem, st>>>(tm, a);
+  count_launch();
+  return launch_status();
+}
+
+template <int FMT, bool SR>
+te_status launch_qtile_any(const void* x, te_dtype in, int64_t R, int64_t C, const TileArgs& a, cudaStream_t st) {
+  if (in == TE_BF16) return launch_qtile<__nv_bfloat16, FMT, SR>(x, R, C, a, st);
+  return launch_qtile<float, FMT, SR>(x, R, C, a, st);
+}
 
 }  // namespace
 }  // namespace te
@@ -661,21 +816,20 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return record_cuda(cudaGetLastError());
   }
   if (rows * cols == 0 && scale_inv_out == nullptr) return TE_OK;
-  // An empty tensor still launches one (load-free) block so that scale_inv_out is published.
-  Fp8Args a{rows, cols, scale, amax_out, compute_scale, fmt == TE_E4M3 ? 448.0f : 57344.0f, q_row, q_col,
-            compute_scale ? nullptr : amax_out, scale_inv_out};
-  const unsigned blocks = patch_blocks(rows, cols, 16, vec_elems(in_dtype, 16));
-  if (in_dtype == TE_BF16) {
-    const auto* p = static_cast<const __nv_bfloat16*>(x);
-    if (fmt == TE_E4M3) fp8_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, a);
-    else fp8_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, a);
-  } else {
-    const auto* p = static_cast<const float*>(x);
-    if (fmt == TE_E4M3) fp8_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, a);
-    else fp8_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, a);
-  }
-  count_launch();
-  return launch_status();
+  // An empty tensor still launches one (load-free) CTA so that scale_inv_out is published.
+  TileArgs a{};
+  a.R = rows;
+  a.C = cols;
+  a.q_row = q_row;
+  a.q_col = q_col;
+  a.scale = scale;
+  a.amax_in = amax_out;
+  a.current = compute_scale;
+  a.fmax = fmt == TE_E4M3 ? 448.0f : 57344.0f;
+  a.amax_out = compute_scale ? nullptr : amax_out;
+  a.scale_inv_out = scale_inv_out;
+  if (fmt == TE_E4M3) return launch_qtile_any<kQE4M3, false>(x, in_dtype, rows, cols, a, st);
+  return launch_qtile_any<kQE5M2, false>(x, in_dtype, rows, cols, a, st);
 }
 
 te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint8_t* q_row,
@@ -690,19 +844,16 @@ te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int6
   if (q_row && (s = zero_scales(s_row, TE_E8M0, rows, cols, st)) != TE_OK) return s;
   if (q_col && (s = zero_scales(s_col, TE_E8M0, cols, rows, st)) != TE_OK) return s;
   if (rows * cols == 0 || (!q_row && !q_col)) return TE_OK;
-  MxArgs a{rows, cols, q_row, s_row, kpad_of(TE_E8M0, cols), q_col, s_col, kpad_of(TE_E8M0, rows)};
-  const int pc = vec_elems(in_dtype, 8);
-  if (q_col) {
-    const unsigned blocks = patch_blocks(rows, cols, 32, pc);
-    if (in_dtype == TE_BF16) mxfp8_kernel<__nv_bfloat16, 32><<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
-    else mxfp8_kernel<float, 32><<<blocks, kThreads, 0, st>>>(static_cast<const float*>(x), a);
-  } else {
-    const unsigned blocks = patch_blocks(rows, cols, 16, pc);
-    if (in_dtype == TE_BF16) mxfp8_kernel<__nv_bfloat16, 16><<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a);
-    else mxfp8_kernel<float, 16><<<blocks, kThreads, 0, st>>>(static_cast<const float*>(x), a);
-  }
-  count_launch();
-  return launch_status();
+  TileArgs a{};
+  a.R = rows;
+  a.C = cols;
+  a.q_row = q_row;
+  a.q_col = q_col;
+  a.s_row = s_row;
+  a.s_col = s_col;
+  a.kpad_row = kpad_of(TE_E8M0, cols);
+  a.kpad_col = kpad_of(TE_E8M0, rows);
+  return launch_qtile_any<kQMX, false>(x, in_dtype, rows, cols, a, st);
 }
 
 te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint32_t flags,
@@ -724,25 +875,28 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   if (row && (s = zero_scales(s_row, TE_UE4M3, rows, cols, st)) != TE_OK) return s;
   if (col && (s = zero_scales(s_col, TE_UE4M3, cols, rows, st)) != TE_OK) return s;
   if (!row && !col) return TE_OK;
-  // An empty tensor launches one load-free block that publishes the S_dec outputs.
-  NvArgs a{rows, cols, flags, rht_signs & 0xFFFFu,
-           static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
-           static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
-           amax, amax_rht, q_row, s_row, gdec_row, kpad_of(TE_UE4M3, cols),
-           q_col, s_col, gdec_col, kpad_of(TE_UE4M3, rows)};
-  const bool sr = (flags & TE_NVFP4_SR) != 0;
-  const unsigned blocks = patch_blocks(rows, cols, 16, vec_elems(in_dtype, 16));
-  if (in_dtype == TE_BF16) {
-    const auto* p = static_cast<const __nv_bfloat16*>(x);
-    if (sr) nvfp4_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, a);
-    else nvfp4_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, a);
-  } else {
-    const auto* p = static_cast<const float*>(x);
-    if (sr) nvfp4_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, a);
-    else nvfp4_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, a);
-  }
-  count_launch();
-  return launch_status();
+  // An empty tensor launches one load-free CTA that publishes the S_dec outputs.
+  TileArgs a{};
+  a.R = rows;
+  a.C = cols;
+  a.q_row = q_row;
+  a.q_col = q_col;
+  a.s_row = s_row;
+  a.s_col = s_col;
+  a.kpad_row = kpad_of(TE_UE4M3, cols);
+  a.kpad_col = kpad_of(TE_UE4M3, rows);
+  a.flags = flags;
+  a.signs = rht_signs & 0xFFFFu;
+  a.seed_lo = static_cast<uint32_t>(seed);
+  a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  a.off_lo = static_cast<uint32_t>(offset);
+  a.off_hi = static_cast<uint32_t>(offset >> 32);
+  a.amax = amax;
+  a.amax_rht = amax_rht;
+  a.gdec_row = gdec_row;
+  a.gdec_col = gdec_col;
+  if (flags & TE_NVFP4_SR) return launch_qtile_any<kQNV, true>(x, in_dtype, rows, cols, a, st);
+  return launch_qtile_any<kQNV, false>(x, in_dtype, rows, cols, a, st);
 }
 
 }  // extern "C"
