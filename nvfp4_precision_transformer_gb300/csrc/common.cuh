@@ -33,6 +33,10 @@ inline te_status launch_status() {
 // [box_rows, 128 bytes] and 128-byte swizzle (the operand tile layout the GEMMs use).
 te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                        uint32_t box_rows);
+// Same with an explicit inner box width in bytes and no swizzle (plain row-major
+// shared-memory boxes, used for the GEMM epilogue's TMA stores).
+te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                             uint32_t box_inner_bytes, uint32_t box_rows);
 
 // Byte offset of logical scale (r, j) in the tensor-core block-scale layout;
 // kpad = number of scale columns after padding (multiple of 4).
@@ -114,6 +118,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// TMA store of a shared-memory box to global (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the shared-memory source of every committed bulk store has been read.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -36,7 +36,9 @@ enum Kind { kBF16 = 0, kFP8 = 1, kMXFP8 = 2, kNVFP4 = 3 };
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int kStages = 4;
+// Scale-factor copies (tcgen05.cp) for the next k-tile are issued before the
+// current k-tile's MMAs, so they do not sit between dependent MMAs.
+constexpr bool kSfLookahead = true;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kGroupM = 8;
@@ -44,6 +46,7 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int KIND>
 struct Cfg {
+  static constexpr int kStages = KIND == kNVFP4 ? 3 : 4;
   static constexpr bool kBlockScaled = KIND >= kMXFP8;
   static constexpr int kAccStages = kBlockScaled ? 1 : 2;
   static constexpr int kABytes = BM * 128;
@@ -59,9 +62,11 @@ struct Cfg {
   static constexpr int kSmemB = kSmemA + kStages * kABytes;
   static constexpr int kSmemSfa = kSmemB + kStages * kBBytes;
   static constexpr int kSmemSfb = kSmemSfa + kStages * kSfaBytes;
-  static constexpr int kSmemBar = kSmemSfb + kStages * kSfbBytes;
+  static constexpr int kSmemStage = kSmemSfb + kStages * kSfbBytes;      // epilogue staging, 2 KB per warp
+  static constexpr int kSmemBar = kSmemStage + kEpiWarps * 2048;
   static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
   static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
+  static_assert(kSmemTotal <= 232448, "shared memory budget");
 };
 
 struct GemmArgs {
@@ -94,8 +99,9 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs args) {
   using C = Cfg<KIND>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -130,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::fence_barrier_init();
     dev::prefetch_tmap(&tmA);
     dev::prefetch_tmap(&tmB);
+    dev::prefetch_tmap(&tmD);
   }
   if (warp == 1) dev::tmem_alloc(tmem_slot, kTmemCols);
   dev::tc_fence_before();
@@ -208,6 +215,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      bool staged = false;  // the current stage's data has arrived and its scales are in TMEM
+      auto sf_slot = [&](int st) {
+        return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
+      };
+      auto copy_sf = [&](int st) {
+        const uint32_t sfa_t = sf_slot(st), sfb_t = sfa_t + C::kSfaCols;
+        const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
+        const uint32_t sfb_s = dev::smem_u32(sSfb + st * C::kSfbBytes);
+#pragma unroll
+        for (int j = 0; j < C::kSfAtoms; ++j) {
+          dev::tc_cp_32x128b_x4(sfa_t + 4 * j, dev::smem_desc(sfa_s + 512 * j, 0, 128, 0));
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            dev::tc_cp_32x128b_x4(sfb_t + 8 * j + 4 * h,
+                                  dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
+        }
+      };
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
@@ -218,28 +242,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
         for (int kt = 0; kt < args.k_tiles; ++kt) {
-          if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
-            ok = false;
-            break;
+          if (!staged) {
+            if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
+              ok = false;
+              break;
+            }
+            dev::tc_fence_after();
+            if (C::kBlockScaled) copy_sf(stage);
           }
-          dev::tc_fence_after();
+          staged = false;
+          const int nstage = stage + 1 == kStages ? 0 : stage + 1;
+          const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
+          if (C::kBlockScaled && kSfLookahead && (kt + 1 < args.k_tiles || tile + static_cast<int>(gridDim.x) < num_tiles)) {
+            if (!dev::mbar_wait(&full[nstage], nphase, abort_flag, args.err)) {
+              ok = false;
+              break;
+            }
+            dev::tc_fence_after();
+            copy_sf(nstage);
+            staged = true;
+          }
           const uint32_t a_addr = dev::smem_u32(sA + stage * C::kABytes);
           const uint32_t b_addr = dev::smem_u32(sB + stage * C::kBBytes);
-          uint32_t sfa_t = 0, sfb_t = 0;
-          if (C::kBlockScaled) {
-            sfa_t = tmem_base + C::kSfTmemBase + stage * (C::kSfaCols + C::kSfbCols);
-            sfb_t = sfa_t + C::kSfaCols;
-            const uint32_t sfa_s = dev::smem_u32(sSfa + stage * C::kSfaBytes);
-            const uint32_t sfb_s = dev::smem_u32(sSfb + stage * C::kSfbBytes);
-#pragma unroll
-            for (int j = 0; j < C::kSfAtoms; ++j) {
-              dev::tc_cp_32x128b_x4(sfa_t + 4 * j, dev::smem_desc(sfa_s + 512 * j, 0, 128, 0));
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                dev::tc_cp_32x128b_x4(sfb_t + 8 * j + 4 * h,
-                                      dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
-            }
-          }
+          const uint32_t sfa_t = sf_slot(stage), sfb_t = sfa_t + C::kSfaCols;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             // K-major: 128-byte rows, 8-row swizzle atoms 1024 B apart; a k-step advances 32 B.
@@ -263,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           dev::tc_commit(&empty[stage]);
-          if (++stage == kStages) stage = 0, phase ^= 1u;
+          stage = nstage;
+          phase = nphase;
         }
         if (!ok) break;
         dev::tc_commit(&acc_full[as]);
@@ -277,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
+    uint8_t* stg = smem + C::kSmemStage + (warp - 2) * 2048;
     const float alpha = (args.alpha_a ? __ldg(args.alpha_a) : 1.0f) * (args.alpha_b ? __ldg(args.alpha_b) : 1.0f);
     int it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
@@ -298,39 +325,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(&acc_empty[as]);
 
-      const int m = mt * BM + quarter * 32 + lane;
+      // Stage 32 rows x 64 bytes at a time in this warp's shared-memory box and write it
+      // with a TMA store (the store clips rows >= M and columns >= N).
+      const int m0 = mt * BM + quarter * 32;
       const int n0 = nt * BN + half * 128;
-      if (m < args.M) {
+      // One 32-row x 64-byte box: lane-row words w[0..15] -> staging buffer -> TMA store.
+      auto store_box = [&](const uint32_t (&w)[16], int nb) {
+        if (lane == 0) dev::bulk_wait_read0();  // the previous box has left the staging buffer
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int j = 0; j < 4; ++j) {
+          const int ch = (j + (lane >> 1)) & 3;  // rotate chunk order: conflict-free 16-byte stores
+          uint32_t v0 = w[0], v1 = w[1], v2 = w[2], v3 = w[3];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 8 columns = 16 bytes of bf16 / 32 bytes of fp32
-            const int n = n0 + 32 * c + 8 * q;
-            if (n >= args.N) continue;
-            float v[8];
+          for (int q = 1; q < 4; ++q)
+            if (ch == q) v0 = w[4 * q], v1 = w[4 * q + 1], v2 = w[4 * q + 2], v3 = w[4 * q + 3];
+          *reinterpret_cast<uint4*>(stg + lane * 64 + ch * 16) = make_uint4(v0, v1, v2, v3);
+        }
+        dev::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          dev::tma_store_2d(&tmD, stg, nb * (args.out_f32 ? 4 : 2), m0);
+          dev::bulk_commit();
+        }
+      };
+      if (m0 < args.M) {
+        if (args.out_f32) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float b = args.bias ? __ldg(args.bias + n + i) : 0.0f;
-              v[i] = __fmaf_rn(__uint_as_float(acc[c][8 * q + i]), alpha, b);
+          for (int bx = 0; bx < 8; ++bx) {
+            const int nb = n0 + bx * 16;
+            if (nb >= args.N) break;
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float b = args.bias ? __ldg(args.bias + nb + i) : 0.0f;
+              w[i] = __float_as_uint(__fmaf_rn(__uint_as_float(acc[bx >> 1][(bx & 1) * 16 + i]), alpha, b));
             }
-            if (args.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.D) + static_cast<int64_t>(m) * args.N + n);
-              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-            } else {
-              uint32_t w[4];
+            store_box(w, nb);
+          }
+        } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.D) + static_cast<int64_t>(m) * args.N + n) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
+          for (int bx = 0; bx < 4; ++bx) {
+            const int nb = n0 + bx * 32;
+            if (nb >= args.N) break;
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float b0 = args.bias ? __ldg(args.bias + nb + 2 * i) : 0.0f;
+              const float b1 = args.bias ? __ldg(args.bias + nb + 2 * i + 1) : 0.0f;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmaf_rn(__uint_as_float(acc[bx][2 * i]), alpha, b0),
+                                                              __fmaf_rn(__uint_as_float(acc[bx][2 * i + 1]), alpha, b1));
+              w[i] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            store_box(w, nb);
           }
         }
       }
     }
+    if (lane == 0) dev::bulk_wait0();
   }
 
   dev::tc_fence_before();
@@ -378,6 +430,10 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   s = b_mn ? make_tmap_2d(&tb, B, static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K), 64)
            : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
   if (s != TE_OK) return s;
+  CUtensorMap td;
+  const uint32_t esize = out == TE_F32 ? 4u : 2u;
+  s = make_tmap_2d_plain(&td, D, static_cast<uint64_t>(N) * esize, static_cast<uint64_t>(M), 64u, 32u);
+  if (s != TE_OK) return s;
   int* err = device_error_word();
   if (err == nullptr) return record_cuda(cudaErrorInvalidDevice);
   GemmArgs g;
@@ -402,7 +458,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.err = err;
   const int tiles = g.m_tiles * g.n_tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<KIND><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, g);
+  gemm_kernel<KIND><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, td, g);
   count_launch();
   return launch_status();
 }

@@ -62,7 +62,8 @@ int num_sms() {
   return g_sms[d];
 }
 
-te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+static te_status encode_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_inner,
+                           uint32_t box_rows, CUtensorMapSwizzle swz) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_encode == nullptr) {
@@ -77,13 +78,22 @@ te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, u
   }
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return record_cuda(cudaErrorInvalidValue);
   return TE_OK;
+}
+
+te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  return encode_2d(map, base, row_bytes, rows, 128u, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                             uint32_t box_inner_bytes, uint32_t box_rows) {
+  return encode_2d(map, base, row_bytes, rows, box_inner_bytes, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace te
