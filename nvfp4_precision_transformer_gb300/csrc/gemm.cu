@@ -36,9 +36,6 @@ enum Kind { kBF16 = 0, kFP8 = 1, kMXFP8 = 2, kNVFP4 = 3 };
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-// Scale-factor copies (tcgen05.cp) for the next k-tile are issued before the
-// current k-tile's MMAs, so they do not sit between dependent MMAs.
-constexpr bool kSfLookahead = true;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kGroupM = 8;
@@ -215,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      bool staged = false;  // the current stage's data has arrived and its scales are in TMEM
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
@@ -242,26 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
         for (int kt = 0; kt < args.k_tiles; ++kt) {
-          if (!staged) {
-            if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
-              ok = false;
-              break;
-            }
-            dev::tc_fence_after();
-            if (C::kBlockScaled) copy_sf(stage);
+          if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
+            ok = false;
+            break;
           }
-          staged = false;
+          dev::tc_fence_after();
+          // Scale factors of this k-tile: smem -> TMEM slot of the stage.  tcgen05.cp and
+          // tcgen05.mma from this thread execute in issue order.
+          if (C::kBlockScaled) copy_sf(stage);
           const int nstage = stage + 1 == kStages ? 0 : stage + 1;
           const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
-          if (C::kBlockScaled && kSfLookahead && (kt + 1 < args.k_tiles || tile + static_cast<int>(gridDim.x) < num_tiles)) {
-            if (!dev::mbar_wait(&full[nstage], nphase, abort_flag, args.err)) {
-              ok = false;
-              break;
-            }
-            dev::tc_fence_after();
-            copy_sf(nstage);
-            staged = true;
-          }
           const uint32_t a_addr = dev::smem_u32(sA + stage * C::kABytes);
           const uint32_t b_addr = dev::smem_u32(sB + stage * C::kBBytes);
           const uint32_t sfa_t = sf_slot(stage), sfb_t = sfa_t + C::kSfaCols;
