@@ -176,7 +176,9 @@ te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int6
  *   key = (seed_lo, seed_hi)), copy_id 0 for the row copy and 1 for the col copy.
  * Outputs: q_row [rows, cols/2] bytes, s_row, gdec_row (device fp32 S_dec);
  *   q_col [cols, rows/2], s_col, gdec_col.  Each triple is nullable as a unit.
- * rows % 16 == 0, cols % 16 == 0; TE_NVFP4_2D excludes TE_NVFP4_RHT_COL. */
+ * cols % 32 == 0 if the row copy is requested, rows % 32 == 0 if the col copy is
+ * (the packed copies' rows must be whole 16-byte units, as the GEMM's K % 32);
+ * TE_NVFP4_2D excludes TE_NVFP4_RHT_COL. */
 te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols,
                             uint32_t flags, uint32_t rht_signs, uint64_t seed, uint64_t offset,
                             const float* amax, const float* amax_rht,

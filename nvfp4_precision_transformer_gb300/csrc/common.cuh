@@ -37,6 +37,10 @@ te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, u
 // shared-memory boxes, used for the GEMM epilogue's TMA stores).
 te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                              uint32_t box_inner_bytes, uint32_t box_rows);
+// Same with the shared-memory box swizzled at its own width (64 B -> 64-byte
+// swizzle, 32 B -> 32-byte swizzle, 16 B -> none).
+te_status make_tmap_2d_boxswz(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                              uint32_t box_inner_bytes, uint32_t box_rows);
 
 // Byte offset of logical scale (r, j) in the tensor-core block-scale layout;
 // kpad = number of scale columns after padding (multiple of 4).

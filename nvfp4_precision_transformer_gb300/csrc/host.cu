@@ -96,6 +96,14 @@ te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_by
   return encode_2d(map, base, row_bytes, rows, box_inner_bytes, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+te_status make_tmap_2d_boxswz(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                              uint32_t box_inner_bytes, uint32_t box_rows) {
+  const CUtensorMapSwizzle swz = box_inner_bytes == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : box_inner_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return encode_2d(map, base, row_bytes, rows, box_inner_bytes, box_rows, swz);
+}
+
 }  // namespace te
 
 namespace {

@@ -317,21 +317,21 @@ __device__ __forceinline__ uint32_t rand16_of(const uint4& w, int k) {  // k-th 
 }
 
 // ---- warp-tile quantizers (FP8, MXFP8, NVFP4) ------------------------------------------------------
-// Persistent CTAs of 8 warps; every warp owns a private 3-stage ring of 64-row x
-// 128-byte tiles (64 x 64 bf16 or 64 x 32 fp32) that its lane 0 fills with TMA
-// (128-byte swizzle), so warps never wait on each other.  Per tile, the row copy
-// is produced by lane l from tile rows l and l + 32 (16-byte shared loads whose
-// swizzled chunks are distinct across each 8-lane phase) and the col copy by lane
-// l from its 4-byte column slice (32 distinct banks per row); each lane then writes
-// whole 64-row / 64-column runs of the copies.  All of a warp's stores of one tile
-// are 16-byte aligned vectors.
+// Persistent CTAs of 8 warps; every warp owns a private 2-stage ring of 64-row x
+// 128-byte input tiles (64 x 64 bf16 or 64 x 32 fp32) that its lane 0 fills with TMA
+// (128-byte swizzle), plus one shared-memory staging box per output copy, so warps
+// never wait on each other.  Per tile, lane l quantizes tile rows l and l + 32 for
+// the row copy (16-byte shared loads, distinct swizzled chunks in every 8-lane
+// phase) and its 4-byte column slice of all 64 rows for the col copy (32 distinct
+// banks per row).  The quantized bytes go to swizzled staging boxes and leave with
+// one TMA bulk-tensor store per copy (the hardware clips the ragged edge); block
+// scales are written directly as contiguous 2-8 byte runs.
 
 enum QFmt { kQE4M3 = 0, kQE5M2 = 1, kQMX = 2, kQNV = 3 };
 
 struct TileArgs {
   int64_t R, C;
-  uint8_t* q_row;
-  uint8_t* q_col;
+  int do_row, do_col;
   // per-tensor FP8
   const float* scale;
   const float* amax_in;
@@ -353,38 +353,30 @@ struct TileArgs {
 };
 
 constexpr int kQWarps = 8;
-constexpr int kQStages = 3;
-constexpr int kQTileBytes = 64 * 128;
-constexpr int kQSmem = kQWarps * kQStages * kQTileBytes + kQWarps * kQStages * 8 + 1024 + 1024;
+constexpr int kQStages = 2;
+constexpr int kQTileBytes = 64 * 128;   // one input tile
+constexpr int kQBoxBytes = 64 * 64;     // one staging box (at most 64 rows x 64 bytes)
+constexpr int kQWarpBytes = kQStages * kQTileBytes + 2 * kQBoxBytes;
+constexpr int kQSmem = kQWarps * kQWarpBytes + 2048 /* barriers + r-tables */ + 1024 /* alignment */;
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 16-byte chunk j of tile row r (128-byte swizzle: chunk j of row r sits at j ^ (r % 8)).
+// 16-byte chunk j of input-tile row r (128-byte swizzle: chunk j of row r sits at j ^ (r % 8)).
 __device__ __forceinline__ uint4 tile_chunk(const uint8_t* tile, int r, int j) {
   return *reinterpret_cast<const uint4*>(tile + r * 128 + ((j ^ (r & 7)) << 4));
 }
-// 4-byte word w (0..31) of tile row r.
+// 4-byte word w (0..31) of input-tile row r.
 __device__ __forceinline__ uint32_t tile_word(const uint8_t* tile, int r, int w) {
   return *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((w >> 2) ^ (r & 7)) << 4) + ((w & 3) << 2));
 }
-
-// 16 consecutive bf16 elements from two 16-byte chunks (c0 holds 0..7, c1 8..15).
-template <typename T>
-__device__ __forceinline__ void unpack16(const uint4& c0, const uint4& c1, float (&v)[16], int) {
-  {
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
+// 16-byte chunk j of row r of a staging box with W-byte rows, in the TMA swizzle
+// of that width (64 B: chunk ^ ((r >> 1) & 3); 32 B: chunk ^ ((r >> 2) & 1); 16 B: none).
+template <int W>
+__device__ __forceinline__ uint4* stage_chunk(uint8_t* box, int r, int j) {
+  const int sw = W == 64 ? ((r >> 1) & 3) : (W == 32 ? ((r >> 2) & 1) : 0);
+  return reinterpret_cast<uint4*>(box + r * W + ((j ^ sw) << 4));
 }
 
 template <int FMT>
-__device__ __forceinline__ uint4 fp8_pack16(const float (&v)[16], float s) {
+__device__ __forceinline__ uint4 fp8_pack16(const float* v, float s) {
   uint32_t w[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -397,13 +389,10 @@ __device__ __forceinline__ uint4 fp8_pack16(const float (&v)[16], float s) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// NVFP4 block of 16 values (block amax bm given): returns 8 packed bytes; *code = scale code.
+// 16 NVFP4 elements with their block's scale multiplier r; rnd0/rnd1 carry the
+// 16-bit random values of elements 0..7 / 8..15 (stochastic rounding).
 template <bool SR>
-__device__ __forceinline__ uint2 nv_block(const float (&v)[16], float bm, float senc, const float* rtab,
-                                          const TileArgs& a, uint64_t g0, uint32_t copy_id, uint32_t* code) {
-  const uint32_t sc = nv_scale_code(bm, senc);
-  *code = sc;
-  const float r = rtab[sc];
+__device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4& rnd0, const uint4& rnd1) {
   uint32_t lo = 0, hi = 0;
   if (!SR) {
 #pragma unroll
@@ -411,16 +400,16 @@ __device__ __forceinline__ uint2 nv_block(const float (&v)[16], float bm, float 
 #pragma unroll
     for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], r), __fmul_rn(v[9 + 2 * j], r)) << (8 * j);
   } else {
-    const uint4 w0 = philox4x32_10(make_uint4(static_cast<uint32_t>(g0 >> 3), copy_id, a.off_lo, a.off_hi),
-                                   a.seed_lo, a.seed_hi);
-    const uint4 w1 = philox4x32_10(make_uint4(static_cast<uint32_t>(g0 >> 3) + 1u, copy_id, a.off_lo, a.off_hi),
-                                   a.seed_lo, a.seed_hi);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], r), rand16_of(w0, k)) << (4 * k);
+    for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], r), rand16_of(rnd0, k)) << (4 * k);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], r), rand16_of(w1, k)) << (4 * k);
+    for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], r), rand16_of(rnd1, k)) << (4 * k);
   }
   return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ uint4 nv_rand(const TileArgs& a, uint64_t g, uint32_t copy_id) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(g >> 3), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
 }
 
 template <int L>
@@ -430,162 +419,195 @@ __device__ __forceinline__ float lanes_max(float v) {
   return v;
 }
 
-// One 64 x 64 bf16 tile.  (The 32-column fp32 tile uses the same code with half
-// of the lanes' column slices; see NCL / NB16.)
-template <typename T, int FMT, bool SR>
-__device__ __forceinline__ void quantize_tile(const uint8_t* tile, int64_t r0, int64_t c0, const TileArgs& a,
-                                              float s_fp8, float senc_r, float senc_c, const float* rtab_r,
-                                              const float* rtab_c, int lane, float& lmax) {
-  constexpr int TC = 128 / sizeof(T);   // tile columns
-  constexpr int NB16 = TC / 16;         // 16-column blocks per tile row
-  const bool two_d = FMT == kQNV && (a.flags & TE_NVFP4_2D) != 0;
-  const bool rht = FMT == kQNV && (a.flags & TE_NVFP4_RHT_COL) != 0;
-  const bool need_max = a.amax_out != nullptr;
+template <typename T, int FMT>
+struct QGeom {
+  static constexpr int TC = 128 / sizeof(T);               // tile columns
+  static constexpr int NB16 = TC / 16;                     // 16-column blocks per tile row
+  static constexpr int NCL = 4 / sizeof(T);                // columns per lane in the col pass
+  static constexpr int ROW_W = FMT == kQNV ? TC / 2 : TC;  // staging row bytes of the row copy
+  static constexpr int COL_W = FMT == kQNV ? 32 : 64;      // staging row bytes of the col copy
+};
 
-  // ---------------- row copy: lane handles tile rows lane and lane + 32
-  if (a.q_row != nullptr) {
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      const int rr = lane + 32 * h;
-      const int64_t row = r0 + rr;
-      float v[NB16][16];
+// Row copy of one tile: lane handles rows lane and lane + 32.
+template <typename T, int FMT, bool SR>
+__device__ __forceinline__ void row_pass(const uint8_t* tile, uint8_t* box, int64_t r0, int64_t c0, const TileArgs& a,
+                                         float s_fp8, float senc, const float* rtab, int lane, float& lmax) {
+  using G = QGeom<T, FMT>;
+  constexpr int NB16 = G::NB16;
+  const bool two_d = FMT == kQNV && (a.flags & TE_NVFP4_2D) != 0;
+  uint32_t codes[2] = {0u, 0u};  // NVFP4 / MXFP8 scale bytes of the two rows
 #pragma unroll
-      for (int j = 0; j < NB16; ++j) {
-        if constexpr (sizeof(T) == 2) {
-          unpack16<T>(tile_chunk(tile, rr, 2 * j), tile_chunk(tile, rr, 2 * j + 1), v[j], 0);
-        } else {
+  for (int h = 0; h < 2; ++h) {
+    const int rr = lane + 32 * h;
+    float v[NB16][16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 c = tile_chunk(tile, rr, 4 * j + q);
-            v[j][4 * q] = __uint_as_float(c.x);
-            v[j][4 * q + 1] = __uint_as_float(c.y);
-            v[j][4 * q + 2] = __uint_as_float(c.z);
-            v[j][4 * q + 3] = __uint_as_float(c.w);
-          }
+    for (int j = 0; j < NB16; ++j) {
+      if constexpr (sizeof(T) == 2) {
+        const uint4 c0v = tile_chunk(tile, rr, 2 * j), c1v = tile_chunk(tile, rr, 2 * j + 1);
+        const uint32_t w[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[j][2 * i] = __uint_as_float(w[i] << 16);
+          v[j][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 c = tile_chunk(tile, rr, 4 * j + q);
+          v[j][4 * q] = __uint_as_float(c.x);
+          v[j][4 * q + 1] = __uint_as_float(c.y);
+          v[j][4 * q + 2] = __uint_as_float(c.z);
+          v[j][4 * q + 3] = __uint_as_float(c.w);
         }
       }
-      float bmax[NB16];
+    }
+    float bmax[NB16];
 #pragma unroll
-      for (int j = 0; j < NB16; ++j) {
-        float m = 0.0f;
+    for (int j = 0; j < NB16; ++j) {
+      float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[j][i]));
-        bmax[j] = m;
-        if (need_max) lmax = fmaxf(lmax, m);
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[j][i]));
+      bmax[j] = m;
+      lmax = fmaxf(lmax, m);
+    }
+    if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
+#pragma unroll
+      for (int j = 0; j < NB16; ++j) *stage_chunk<G::ROW_W>(box, rr, j) = fp8_pack16<FMT>(v[j], s_fp8);
+    } else if constexpr (FMT == kQMX) {
+#pragma unroll
+      for (int j = 0; j < NB16; j += 2) {
+        const int E = mx_exponent(fmaxf(bmax[j], bmax[j + 1]));
+        const float mult = mx_mult(E);
+        *stage_chunk<G::ROW_W>(box, rr, j) = fp8_pack16<kQE4M3>(v[j], mult);
+        *stage_chunk<G::ROW_W>(box, rr, j + 1) = fp8_pack16<kQE4M3>(v[j + 1], mult);
+        codes[h] |= static_cast<uint32_t>(E + 127) << (8 * (j / 2));
       }
+    } else {
       if (two_d) {
 #pragma unroll
         for (int j = 0; j < NB16; ++j) bmax[j] = lanes_max<16>(bmax[j]);  // 16 rows x 16 cols
       }
-      const bool row_ok = row < a.R;
-      if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
-        if (row_ok) {
+      uint4 rnd[2 * NB16];
+      const uint64_t g = static_cast<uint64_t>(r0 + rr) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(c0);
 #pragma unroll
-          for (int j = 0; j < NB16; ++j)
-            if (c0 + 16 * j < a.C)
-              *reinterpret_cast<uint4*>(a.q_row + row * a.C + c0 + 16 * j) = fp8_pack16<FMT>(v[j], s_fp8);
-        }
-      } else if constexpr (FMT == kQMX) {
-        // blocks of 32 = pairs of 16-blocks
+      for (int k = 0; k < 2 * NB16; ++k) rnd[k] = SR ? nv_rand(a, g + 8 * k, 0u) : make_uint4(0, 0, 0, 0);
+      uint2 q[NB16];
 #pragma unroll
-        for (int j = 0; j < NB16; j += 2) {
-          const int E = mx_exponent(fmaxf(bmax[j], bmax[j + 1]));
-          const float mult = mx_mult(E);
-          if (row_ok && c0 + 16 * j < a.C) {
-            uint4* dst = reinterpret_cast<uint4*>(a.q_row + row * a.C + c0 + 16 * j);
-            dst[0] = fp8_pack16<kQE4M3>(v[j], mult);
-            dst[1] = fp8_pack16<kQE4M3>(v[j + 1], mult);
-            a.s_row[scale_offset(row, (c0 + 16 * j) / 32, a.kpad_row)] = static_cast<uint8_t>(E + 127);
-          }
-        }
-      } else {
-        uint32_t codes = 0;
+      for (int j = 0; j < NB16; ++j) {
+        const uint32_t sc = nv_scale_code(bmax[j], senc);
+        codes[h] |= sc << (8 * j);
+        q[j] = nv_pack16<SR>(v[j], rtab[sc], rnd[2 * j], rnd[2 * j + 1]);
+      }
 #pragma unroll
-        for (int j = 0; j < NB16; ++j) {
-          uint32_t sc;
-          const uint64_t g0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(c0 + 16 * j);
-          const uint2 q = nv_block<SR>(v[j], bmax[j], senc_r, rtab_r, a, g0, 0u, &sc);
-          codes |= sc << (8 * j);
-          if (row_ok && c0 + 16 * j < a.C)
-            *reinterpret_cast<uint2*>(a.q_row + row * (a.C / 2) + (c0 + 16 * j) / 2) = q;
-        }
-        if (row_ok) {
-          uint8_t* sdst = a.s_row + scale_offset(row, c0 / 16, a.kpad_row);
-          if (NB16 == 4) *reinterpret_cast<uint32_t*>(sdst) = codes;
-          else *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(codes);
-        }
+      for (int j = 0; j < NB16; j += 2)
+        *stage_chunk<G::ROW_W>(box, rr, j / 2) = make_uint4(q[j].x, q[j].y, q[j + 1].x, q[j + 1].y);
+    }
+  }
+  if constexpr (FMT == kQNV || FMT == kQMX) {
+    // rows r0 + lane and r0 + lane + 32 share a 16-byte row of the scale atom, 4 bytes apart
+    const int64_t row = r0 + lane;
+    if (row < a.R) {
+      const int64_t jb = FMT == kQNV ? c0 / 16 : c0 / 32;
+      uint8_t* dst = a.s_row + scale_offset(row, jb, a.kpad_row);
+      const bool both = row + 32 < a.R;
+      if constexpr (FMT == kQNV && NB16 == 4) {
+        if (both) *reinterpret_cast<uint2*>(dst) = make_uint2(codes[0], codes[1]);
+        else *reinterpret_cast<uint32_t*>(dst) = codes[0];
+      } else if constexpr (FMT == kQNV || (FMT == kQMX && NB16 == 4)) {   // 2 scale bytes per row
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes[0]);
+        if (both) *reinterpret_cast<uint16_t*>(dst + 4) = static_cast<uint16_t>(codes[1]);
+      } else {                                                            // 1 scale byte per row
+        dst[0] = static_cast<uint8_t>(codes[0]);
+        if (both) dst[4] = static_cast<uint8_t>(codes[1]);
       }
     }
   }
+}
 
-  // ---------------- col copy: lane handles the 4-byte column slice `lane` (2 bf16 / 1 fp32 columns)
-  if (a.q_col != nullptr) {
-    constexpr int NCL = 4 / sizeof(T);
-    constexpr int RB = FMT == kQMX ? 32 : 16;   // rows per col-copy block
+// Col copy of one tile: lane handles its 4-byte column slice (NCL columns) of all 64 rows.
+template <typename T, int FMT, bool SR>
+__device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int64_t r0, int64_t c0, const TileArgs& a,
+                                         float s_fp8, float senc, const float* rtab, int lane, float& lmax,
+                                         bool track_max) {
+  using G = QGeom<T, FMT>;
+  constexpr int NCL = G::NCL;
+  const bool two_d = FMT == kQNV && (a.flags & TE_NVFP4_2D) != 0;
+  const bool rht = FMT == kQNV && (a.flags & TE_NVFP4_RHT_COL) != 0;
+  uint32_t codes[NCL] = {};
+  constexpr int RB = FMT == kQMX ? 32 : 16;  // rows per block of the col copy
 #pragma unroll 1
-    for (int b = 0; b < 64 / RB; ++b) {
-      float v[NCL][RB];
+  for (int b = 0; b < 64 / RB; ++b) {
+    float v[NCL][RB];
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        const uint32_t w = tile_word(tile, b * RB + r, lane);
-        if constexpr (sizeof(T) == 2) {
-          v[0][r] = __uint_as_float(w << 16);
-          v[NCL - 1][r] = __uint_as_float(w & 0xFFFF0000u);
-        } else {
-          v[0][r] = __uint_as_float(w);
-        }
+    for (int r = 0; r < RB; ++r) {
+      const uint32_t w = tile_word(tile, b * RB + r, lane);
+      if constexpr (sizeof(T) == 2) {
+        v[0][r] = __uint_as_float(w << 16);
+        v[NCL - 1][r] = __uint_as_float(w & 0xFFFF0000u);
+      } else {
+        v[0][r] = __uint_as_float(w);
       }
-      const int64_t rb0 = r0 + b * RB;
-      const bool rows_ok = rb0 < a.R;
+    }
+    float tile_m = 0.0f;
+    if (two_d) {
 #pragma unroll
-      for (int q = 0; q < NCL; ++q) {
-        const int64_t col = c0 + lane * NCL + q;
-        const bool ok = rows_ok && col < a.C;
-        if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
-          if (need_max && a.q_row == nullptr)
+      for (int qq = 0; qq < NCL; ++qq)
 #pragma unroll
-            for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
-          if (ok) *reinterpret_cast<uint4*>(a.q_col + col * a.R + rb0) = fp8_pack16<FMT>(v[q], s_fp8);
-        } else if constexpr (FMT == kQMX) {
-          float m = 0.0f;
+        for (int r = 0; r < RB; ++r) tile_m = fmaxf(tile_m, fabsf(v[qq][r]));
+      tile_m = lanes_max<16 / NCL>(tile_m);  // 16 rows x 16 columns
+    }
 #pragma unroll
-          for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
-          const int E = mx_exponent(m);
-          const float mult = mx_mult(E);
-          if (ok) {
-            float h0[16], h1[16];
+    for (int q = 0; q < NCL; ++q) {
+      const int cl = lane * NCL + q;  // column within the tile = row of the col-copy box
+      if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
+        if (track_max)
 #pragma unroll
-            for (int r = 0; r < 16; ++r) h0[r] = v[q][r], h1[r] = v[q][16 + r];
-            uint4* dst = reinterpret_cast<uint4*>(a.q_col + col * a.R + rb0);
-            dst[0] = fp8_pack16<kQE4M3>(h0, mult);
-            dst[1] = fp8_pack16<kQE4M3>(h1, mult);
-            a.s_col[scale_offset(col, rb0 / 32, a.kpad_col)] = static_cast<uint8_t>(E + 127);
-          }
-        } else {
-          float x[16];
+          for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
+        *stage_chunk<G::COL_W>(box, cl, b) = fp8_pack16<FMT>(v[q], s_fp8);
+      } else if constexpr (FMT == kQMX) {
+        float m = 0.0f;
 #pragma unroll
-          for (int r = 0; r < 16; ++r) x[r] = v[q][r];
-          if (rht) rht16(x, a.signs);
-          float m = 0.0f;
+        for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
+        const int E = mx_exponent(m);
+        const float mult = mx_mult(E);
+        *stage_chunk<G::COL_W>(box, cl, 2 * b) = fp8_pack16<kQE4M3>(&v[q][0], mult);
+        *stage_chunk<G::COL_W>(box, cl, 2 * b + 1) = fp8_pack16<kQE4M3>(&v[q][16], mult);
+        codes[q] |= static_cast<uint32_t>(E + 127) << (8 * b);
+      } else {
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = v[q][r];
+        if (rht) rht16(x, a.signs);
+        float m = tile_m;
+        if (!two_d) {
+          m = 0.0f;
 #pragma unroll
           for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(x[r]));
-          if (two_d) {
-            // 16 x 16 tile amax: the tile's 16 columns are spread over 16 / NCL lanes
-            float m2 = 0.0f;
-#pragma unroll
-            for (int qq = 0; qq < NCL; ++qq)
-#pragma unroll
-              for (int r = 0; r < 16; ++r) m2 = fmaxf(m2, fabsf(v[qq][r]));
-            m = lanes_max<16 / NCL>(m2);
-          }
-          uint32_t sc;
-          const uint64_t g0 = static_cast<uint64_t>(col) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(rb0);
-          const uint2 qv = nv_block<SR>(x, m, senc_c, rtab_c, a, g0, 1u, &sc);
-          if (ok) {
-            *reinterpret_cast<uint2*>(a.q_col + col * (a.R / 2) + rb0 / 2) = qv;
-            a.s_col[scale_offset(col, rb0 / 16, a.kpad_col)] = static_cast<uint8_t>(sc);
-          }
         }
+        const uint32_t sc = nv_scale_code(m, senc);
+        codes[q] |= sc << (8 * b);
+        uint4 r0v = make_uint4(0, 0, 0, 0), r1v = r0v;
+        if (SR) {
+          const uint64_t g = static_cast<uint64_t>(c0 + cl) * static_cast<uint64_t>(a.R) +
+                             static_cast<uint64_t>(r0 + b * 16);
+          r0v = nv_rand(a, g, 1u);
+          r1v = nv_rand(a, g + 8, 1u);
+        }
+        const uint2 qv = nv_pack16<SR>(x, rtab[sc], r0v, r1v);
+        // two 16-row blocks share one 16-byte chunk of the 32-byte box row
+        uint8_t* dst = reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, cl, b >> 1)) + (b & 1) * 8;
+        *reinterpret_cast<uint2*>(dst) = qv;
+      }
+    }
+  }
+  if constexpr (FMT == kQNV || FMT == kQMX) {
+#pragma unroll
+    for (int q = 0; q < NCL; ++q) {
+      const int64_t col = c0 + lane * NCL + q;
+      if (col < a.C) {
+        uint8_t* dst = a.s_col + scale_offset(col, FMT == kQNV ? r0 / 16 : r0 / 32, a.kpad_col);
+        if constexpr (FMT == kQNV) *reinterpret_cast<uint32_t*>(dst) = codes[q];
+        else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes[q]);
       }
     }
   }
@@ -593,22 +615,26 @@ __device__ __forceinline__ void quantize_tile(const uint8_t* tile, int64_t r0, i
 
 template <typename T, int FMT, bool SR>
 __global__ void __launch_bounds__(kQWarps * 32, 1)
-    qtile_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ TileArgs a) {
-  constexpr int TC = 128 / sizeof(T);
+    qtile_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_row,
+                 const __grid_constant__ CUtensorMap tm_col, const __grid_constant__ TileArgs a) {
+  using G = QGeom<T, FMT>;
+  constexpr int TC = G::TC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = smem + warp * kQStages * kQTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQWarps * kQStages * kQTileBytes) + warp * kQStages;
-  float* rtab = reinterpret_cast<float*>(smem + kQWarps * kQStages * kQTileBytes + kQWarps * kQStages * 8);
+  uint8_t* ring = smem + warp * kQWarpBytes;
+  uint8_t* box_row = ring + kQStages * kQTileBytes;
+  uint8_t* box_col = box_row + kQBoxBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQWarps * kQWarpBytes) + warp * kQStages;
+  float* rtab = reinterpret_cast<float*>(smem + kQWarps * kQWarpBytes + 256);
 
   float s_fp8 = 1.0f, senc_r = 1.0f, senc_c = 1.0f;
   if (FMT == kQE4M3 || FMT == kQE5M2) s_fp8 = a.current ? current_scale(*a.amax_in, a.fmax) : *a.scale;
   if (FMT == kQNV) {
     const bool rht = (a.flags & TE_NVFP4_RHT_COL) != 0;
-    if (a.q_row != nullptr) senc_r = nv_senc(*a.amax);
-    if (a.q_col != nullptr) senc_c = nv_senc(rht ? *a.amax_rht : *a.amax);
+    if (a.do_row) senc_r = nv_senc(*a.amax);
+    if (a.do_col) senc_c = nv_senc(rht ? *a.amax_rht : *a.amax);
     if (threadIdx.x < 128) {
       const float dv = ue4m3_value(threadIdx.x);
       rtab[threadIdx.x] = dv > 0.0f ? __fdiv_rn(senc_r, dv) : 0.0f;
@@ -636,7 +662,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       const int64_t t = first + s * W;
       if (t < n) {
         dev::mbar_expect_tx(&bars[s], kQTileBytes);
-        dev::tma_load_2d(ring + s * kQTileBytes, &tm, &bars[s], static_cast<int>((t % tiles_c) * 128),
+        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>((t % tiles_c) * 128),
                          static_cast<int>((t / tiles_c) * 64));
       }
     }
@@ -648,19 +674,28 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
     const int s = k % kQStages;
     const uint32_t ph = static_cast<uint32_t>(k / kQStages) & 1u;
     if (!dev::mbar_wait(&bars[s], ph, &abort_flag, a.err)) break;
-    quantize_tile<T, FMT, SR>(ring + s * kQTileBytes, (t / tiles_c) * 64, (t % tiles_c) * TC, a, s_fp8, senc_r,
-                              senc_c, rtab, rtab + 128, lane, lmax);
+    const int64_t r0 = (t / tiles_c) * 64, c0 = (t % tiles_c) * TC;
+    const uint8_t* tile = ring + s * kQTileBytes;
+    if (lane == 0) dev::bulk_wait_read0();  // the previous tile's boxes have been read out
     __syncwarp();
-    fence_proxy_async_smem();
-    const int64_t nt = t + kQStages * W;
-    if (lane == 0 && nt < n) {
-      dev::mbar_expect_tx(&bars[s], kQTileBytes);
-      dev::tma_load_2d(ring + s * kQTileBytes, &tm, &bars[s], static_cast<int>((nt % tiles_c) * 128),
-                       static_cast<int>((nt / tiles_c) * 64));
+    if (a.do_row) row_pass<T, FMT, SR>(tile, box_row, r0, c0, a, s_fp8, senc_r, rtab, lane, lmax);
+    if (a.do_col) col_pass<T, FMT, SR>(tile, box_col, r0, c0, a, s_fp8, senc_c, rtab + 128, lane, lmax, !a.do_row);
+    dev::fence_proxy_async();  // order this tile's shared-memory reads and box writes before the async copies
+    __syncwarp();
+    if (lane == 0) {
+      if (a.do_row) dev::tma_store_2d(&tm_row, box_row, static_cast<int>(c0 * G::ROW_W / TC), static_cast<int>(r0));
+      if (a.do_col) dev::tma_store_2d(&tm_col, box_col, static_cast<int>(r0 * G::COL_W / 64), static_cast<int>(c0));
+      dev::bulk_commit();
+      const int64_t nt = t + kQStages * W;
+      if (nt < n) {
+        dev::mbar_expect_tx(&bars[s], kQTileBytes);
+        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>((nt % tiles_c) * 128),
+                         static_cast<int>((nt / tiles_c) * 64));
+      }
     }
   }
   if (abort_flag) {
-    // bounded wait for this warp's own copies still in flight before the CTA exits
+    // bounded wait for this warp's own loads still in flight before the CTA exits
     int dummy = 0;
     for (int j = 0; j < kQStages; ++j) {
       const int kk = k + j;
@@ -668,6 +703,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       if (t < n) dev::mbar_wait(&bars[kk % kQStages], static_cast<uint32_t>(kk / kQStages) & 1u, &dummy, a.err);
     }
   }
+  if (lane == 0) dev::bulk_wait0();
   if ((FMT == kQE4M3 || FMT == kQE5M2) && a.amax_out != nullptr) {
     lmax = warp_max(lmax);
     if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(a.amax_out), __float_as_uint(lmax));
@@ -727,7 +763,9 @@ inline int64_t kpad_of(te_dtype fmt, int64_t cols) {
 
 
 template <typename T, int FMT, bool SR>
-te_status launch_qtile(const void* x, int64_t R, int64_t C, TileArgs a, cudaStream_t st) {
+te_status launch_qtile(const void* x, int64_t R, int64_t C, uint8_t* q_row, uint8_t* q_col, TileArgs a,
+                       cudaStream_t st) {
+  using G = QGeom<T, FMT>;
   static bool attr_set[64] = {false};
   int dev_id = 0;
   cudaGetDevice(&dev_id);
@@ -737,28 +775,39 @@ te_status launch_qtile(const void* x, int64_t R, int64_t C, TileArgs a, cudaStre
       return record_cuda(cudaGetLastError());
     attr_set[dev_id] = true;
   }
-  CUtensorMap tm;
-  memset(&tm, 0, sizeof(tm));
+  CUtensorMap tin, trow, tcol;
+  memset(&tin, 0, sizeof(tin));
+  memset(&trow, 0, sizeof(trow));
+  memset(&tcol, 0, sizeof(tcol));
+  a.do_row = q_row != nullptr;
+  a.do_col = q_col != nullptr;
   if (R * C > 0) {
-    te_status s = make_tmap_2d(&tm, x, static_cast<uint64_t>(C) * sizeof(T), static_cast<uint64_t>(R), 64);
+    te_status s = make_tmap_2d(&tin, x, static_cast<uint64_t>(C) * sizeof(T), static_cast<uint64_t>(R), 64);
+    if (s == TE_OK && q_row)
+      s = make_tmap_2d_boxswz(&trow, q_row, static_cast<uint64_t>(FMT == kQNV ? C / 2 : C), static_cast<uint64_t>(R),
+                              G::ROW_W, 64);
+    if (s == TE_OK && q_col)
+      s = make_tmap_2d_boxswz(&tcol, q_col, static_cast<uint64_t>(FMT == kQNV ? R / 2 : R), static_cast<uint64_t>(C),
+                              G::COL_W, G::TC);
     if (s != TE_OK) return s;
   }
   a.err = device_error_word();
   if (a.err == nullptr) return record_cuda(cudaErrorInvalidDevice);
-  constexpr int TC = 128 / sizeof(T);
+  constexpr int TC = G::TC;
   const int64_t tiles = ((R + 63) / 64) * ((C + TC - 1) / TC);
   int64_t grid = (tiles + kQWarps - 1) / kQWarps;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), kQWarps * 32, kQSmem, st>>>(tm, a);
+  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), kQWarps * 32, kQSmem, st>>>(tin, trow, tcol, a);
   count_launch();
   return launch_status();
 }
 
 template <int FMT, bool SR>
-te_status launch_qtile_any(const void* x, te_dtype in, int64_t R, int64_t C, const TileArgs& a, cudaStream_t st) {
-  if (in == TE_BF16) return launch_qtile<__nv_bfloat16, FMT, SR>(x, R, C, a, st);
-  return launch_qtile<float, FMT, SR>(x, R, C, a, st);
+te_status launch_qtile_any(const void* x, te_dtype in, int64_t R, int64_t C, uint8_t* q_row, uint8_t* q_col,
+                           const TileArgs& a, cudaStream_t st) {
+  if (in == TE_BF16) return launch_qtile<__nv_bfloat16, FMT, SR>(x, R, C, q_row, q_col, a, st);
+  return launch_qtile<float, FMT, SR>(x, R, C, q_row, q_col, a, st);
 }
 
 }  // namespace
@@ -820,16 +869,14 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
   TileArgs a{};
   a.R = rows;
   a.C = cols;
-  a.q_row = q_row;
-  a.q_col = q_col;
   a.scale = scale;
   a.amax_in = amax_out;
   a.current = compute_scale;
   a.fmax = fmt == TE_E4M3 ? 448.0f : 57344.0f;
   a.amax_out = compute_scale ? nullptr : amax_out;
   a.scale_inv_out = scale_inv_out;
-  if (fmt == TE_E4M3) return launch_qtile_any<kQE4M3, false>(x, in_dtype, rows, cols, a, st);
-  return launch_qtile_any<kQE5M2, false>(x, in_dtype, rows, cols, a, st);
+  if (fmt == TE_E4M3) return launch_qtile_any<kQE4M3, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
+  return launch_qtile_any<kQE5M2, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
 }
 
 te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint8_t* q_row,
@@ -847,13 +894,11 @@ te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int6
   TileArgs a{};
   a.R = rows;
   a.C = cols;
-  a.q_row = q_row;
-  a.q_col = q_col;
   a.s_row = s_row;
   a.s_col = s_col;
   a.kpad_row = kpad_of(TE_E8M0, cols);
   a.kpad_col = kpad_of(TE_E8M0, rows);
-  return launch_qtile_any<kQMX, false>(x, in_dtype, rows, cols, a, st);
+  return launch_qtile_any<kQMX, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
 }
 
 te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint32_t flags,
@@ -869,6 +914,7 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   if (col != (s_col != nullptr) || col != (gdec_col != nullptr)) return TE_ERR_NULL;
   if ((row || (col && !(flags & TE_NVFP4_RHT_COL))) && amax == nullptr) return TE_ERR_NULL;
   if (col && (flags & TE_NVFP4_RHT_COL) && amax_rht == nullptr) return TE_ERR_NULL;
+  if ((row && cols % 32) || (col && rows % 32)) return TE_ERR_SHAPE;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) || (col && (!aligned16(q_col) || !aligned16(s_col))))
     return TE_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -879,8 +925,6 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   TileArgs a{};
   a.R = rows;
   a.C = cols;
-  a.q_row = q_row;
-  a.q_col = q_col;
   a.s_row = s_row;
   a.s_col = s_col;
   a.kpad_row = kpad_of(TE_UE4M3, cols);
@@ -895,8 +939,8 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   a.amax_rht = amax_rht;
   a.gdec_row = gdec_row;
   a.gdec_col = gdec_col;
-  if (flags & TE_NVFP4_SR) return launch_qtile_any<kQNV, true>(x, in_dtype, rows, cols, a, st);
-  return launch_qtile_any<kQNV, false>(x, in_dtype, rows, cols, a, st);
+  if (flags & TE_NVFP4_SR) return launch_qtile_any<kQNV, true>(x, in_dtype, rows, cols, q_row, q_col, a, st);
+  return launch_qtile_any<kQNV, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
 }
 
 }  // extern "C"

@@ -148,6 +148,13 @@ def test_fp8_full_size_sampled():
     G.assert_equal_codes(q_col[cols], Q.fp8_cast(np.ascontiguousarray(x32[:, cols].T), cs, "e4m3"), "col sample")
 
 
+def test_nvfp4_rejects_non_32_dims():
+    x = torch.zeros(48, 64, dtype=torch.bfloat16, device=G.DEV)
+    with pytest.raises(te.TEError) as ei:
+        G.nvfp4(x, 0, row=False, col=True)     # col copy contracts over 48 rows
+    assert ei.value.status == 2
+
+
 def test_fp8_rejects_bad_shapes():
     x = torch.zeros(24, 32, dtype=torch.bfloat16, device=G.DEV)
     with pytest.raises(te.TEError) as ei:
@@ -201,7 +208,7 @@ def test_mxfp8_full_size_sampled():
 
 # ---- NVFP4 ---------------------------------------------------------------------------------------------
 
-NV_SHAPES = [(48, 80), (1024, 768), (272, 208), (16, 16)]
+NV_SHAPES = [(64, 96), (1024, 768), (288, 224), (32, 32)]
 
 
 def _nv_expect(x32, flags, signs, seed, offset):
@@ -253,7 +260,7 @@ def test_nvfp4_e2m1_encoder_structured_values():
     vals = (bits[:, None] | low[None, :]).reshape(-1).view(np.float32)
     vals = np.concatenate([vals, np.array([5.0, 5.5, 6.0, 7.0, -5.0, -0.0, 0.25, 0.75], np.float32)])
     vals = np.clip(vals, -6.0, 6.0)
-    nb = (vals.size // 15 // 64) * 64                      # whole [16 x 64] tiles of blocks
+    nb = (vals.size // 15 // 128) * 128                    # whole [32 x 64] tiles of blocks
     blocks = vals[: nb * 15].reshape(nb, 15)
     blocks = np.concatenate([np.full((nb, 1), 6.0, np.float32), blocks], axis=1)
     z = blocks.reshape(nb // 4, 64)
