@@ -68,9 +68,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;  // one 32x32 -> 64-bit multiply each
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
   }
   return c;
 }
@@ -242,14 +243,16 @@ inline unsigned patch_blocks(int64_t rows, int64_t cols, int pr, int pc) {
 // ---- amax ---------------------------------------------------------------------------------------
 template <typename T, bool RHT>
 __global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C, float* amax,
-                                                        float* amax_rht, uint32_t signs) {
-  Patch<T, 16, 16> p;
+                                                           float* amax_rht, uint32_t signs) {
+  // the rotated amax transforms every column of the patch: 8-byte row vectors halve its registers
+  using P = Patch<T, RHT ? 8 : 16, 16>;
+  P p;
   p.load(x, R, C);
   block_max_to(p.absmax(), amax);
   if (RHT) {
     float mr = 0.0f;
 #pragma unroll
-    for (int i = 0; i < Patch<T, 16, 16>::PC; ++i) {
+    for (int i = 0; i < P::PC; ++i) {
       float col[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) col[r] = p.at(r, i);
@@ -352,12 +355,7 @@ struct TileArgs {
   int* err;
 };
 
-constexpr int kQWarps = 8;
-constexpr int kQStages = 2;
 constexpr int kQTileBytes = 64 * 128;   // one input tile
-constexpr int kQBoxBytes = 64 * 64;     // one staging box (at most 64 rows x 64 bytes)
-constexpr int kQWarpBytes = kQStages * kQTileBytes + 2 * kQBoxBytes;
-constexpr int kQSmem = kQWarps * kQWarpBytes + 2048 /* barriers + r-tables */ + 1024 /* alignment */;
 
 // 16-byte chunk j of input-tile row r (128-byte swizzle: chunk j of row r sits at j ^ (r % 8)).
 __device__ __forceinline__ uint4 tile_chunk(const uint8_t* tile, int r, int j) {
@@ -426,6 +424,26 @@ struct QGeom {
   static constexpr int NCL = 4 / sizeof(T);                // columns per lane in the col pass
   static constexpr int ROW_W = FMT == kQNV ? TC / 2 : TC;  // staging row bytes of the row copy
   static constexpr int COL_W = FMT == kQNV ? 32 : 64;      // staging row bytes of the col copy
+  static constexpr int ROW_BOX = 64 * ROW_W;               // staging box bytes of the row copy
+  static constexpr int COL_BOX = TC * COL_W;               // staging box bytes of the col copy
+};
+
+// Warps per CTA and input stages per warp.  The stochastic-rounding NVFP4 kernel is
+// arithmetic-bound (Philox + rounding per element), so it trades the second stage
+// for twice the warps; every other configuration is bandwidth-bound.
+template <int FMT, bool SR>
+struct QLaunch {
+  static constexpr int NW = (FMT == kQNV && SR) ? 16 : 8;
+  static constexpr int NS = (FMT == kQNV && SR) ? 1 : 2;
+};
+template <typename T, int FMT, bool SR>
+struct QSmem {
+  using G = QGeom<T, FMT>;
+  using Lc = QLaunch<FMT, SR>;
+  static constexpr int kWarpBytes = Lc::NS * kQTileBytes + G::ROW_BOX + G::COL_BOX;
+  static constexpr int kTotal = Lc::NW * kWarpBytes + 2048 /* barriers + r-tables */ + 1024 /* alignment */;
+  static_assert(kTotal <= 232448, "shared memory budget");
+  static_assert(G::ROW_BOX % 1024 == 0 && G::COL_BOX % 1024 == 0, "box alignment");
 };
 
 // Row copy of one tile: lane handles rows lane and lane + 32.
@@ -487,16 +505,18 @@ __device__ __forceinline__ void row_pass(const uint8_t* tile, uint8_t* box, int6
 #pragma unroll
         for (int j = 0; j < NB16; ++j) bmax[j] = lanes_max<16>(bmax[j]);  // 16 rows x 16 cols
       }
-      uint4 rnd[2 * NB16];
       const uint64_t g = static_cast<uint64_t>(r0 + rr) * static_cast<uint64_t>(a.C) + static_cast<uint64_t>(c0);
-#pragma unroll
-      for (int k = 0; k < 2 * NB16; ++k) rnd[k] = SR ? nv_rand(a, g + 8 * k, 0u) : make_uint4(0, 0, 0, 0);
       uint2 q[NB16];
 #pragma unroll
       for (int j = 0; j < NB16; ++j) {
         const uint32_t sc = nv_scale_code(bmax[j], senc);
         codes[h] |= sc << (8 * j);
-        q[j] = nv_pack16<SR>(v[j], rtab[sc], rnd[2 * j], rnd[2 * j + 1]);
+        uint4 rnd0 = make_uint4(0, 0, 0, 0), rnd1 = rnd0;
+        if (SR) {
+          rnd0 = nv_rand(a, g + 16 * j, 0u);
+          rnd1 = nv_rand(a, g + 16 * j + 8, 0u);
+        }
+        q[j] = nv_pack16<SR>(v[j], rtab[sc], rnd0, rnd1);
       }
 #pragma unroll
       for (int j = 0; j < NB16; j += 2)
@@ -614,18 +634,21 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
 }
 
 template <typename T, int FMT, bool SR>
-__global__ void __launch_bounds__(kQWarps * 32, 1)
+__global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
     qtile_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_row,
                  const __grid_constant__ CUtensorMap tm_col, const __grid_constant__ TileArgs a) {
   using G = QGeom<T, FMT>;
   constexpr int TC = G::TC;
+  constexpr int kQWarps = QLaunch<FMT, SR>::NW;
+  constexpr int kQStages = QLaunch<FMT, SR>::NS;
+  constexpr int kQWarpBytes = QSmem<T, FMT, SR>::kWarpBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + warp * kQWarpBytes;
   uint8_t* box_row = ring + kQStages * kQTileBytes;
-  uint8_t* box_col = box_row + kQBoxBytes;
+  uint8_t* box_col = box_row + G::ROW_BOX;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQWarps * kQWarpBytes) + warp * kQStages;
   float* rtab = reinterpret_cast<float*>(smem + kQWarps * kQWarpBytes + 256);
 
@@ -736,14 +759,20 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
   if (rows * cols == 0) return TE_OK;
   if (in == TE_BF16) {
     const auto* p = static_cast<const __nv_bfloat16*>(x);
-    const unsigned blocks = patch_blocks(rows, cols, 16, 8);
-    if (amax_rht) amax_kernel<__nv_bfloat16, true><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
-    else amax_kernel<__nv_bfloat16, false><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, nullptr, signs);
+    if (amax_rht)
+      amax_kernel<__nv_bfloat16, true><<<patch_blocks(rows, cols, 16, 4), kThreads, 0, st>>>(p, rows, cols, amax,
+                                                                                           amax_rht, signs);
+    else
+      amax_kernel<__nv_bfloat16, false><<<patch_blocks(rows, cols, 16, 8), kThreads, 0, st>>>(p, rows, cols, amax,
+                                                                                            nullptr, signs);
   } else {
     const auto* p = static_cast<const float*>(x);
-    const unsigned blocks = patch_blocks(rows, cols, 16, 4);
-    if (amax_rht) amax_kernel<float, true><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
-    else amax_kernel<float, false><<<blocks, kThreads, 0, st>>>(p, rows, cols, amax, nullptr, signs);
+    if (amax_rht)
+      amax_kernel<float, true><<<patch_blocks(rows, cols, 16, 2), kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
+                                                                                   signs);
+    else
+      amax_kernel<float, false><<<patch_blocks(rows, cols, 16, 4), kThreads, 0, st>>>(p, rows, cols, amax, nullptr,
+                                                                                    signs);
   }
   count_launch();
   return launch_status();
@@ -770,8 +799,8 @@ te_status launch_qtile(const void* x, int64_t R, int64_t C, uint8_t* q_row, uint
   int dev_id = 0;
   cudaGetDevice(&dev_id);
   if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
-    if (cudaFuncSetAttribute(qtile_kernel<T, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(qtile_kernel<T, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QSmem<T, FMT, SR>::kTotal) != cudaSuccess)
       return record_cuda(cudaGetLastError());
     attr_set[dev_id] = true;
   }
@@ -794,11 +823,13 @@ te_status launch_qtile(const void* x, int64_t R, int64_t C, uint8_t* q_row, uint
   a.err = device_error_word();
   if (a.err == nullptr) return record_cuda(cudaErrorInvalidDevice);
   constexpr int TC = G::TC;
+  constexpr int NW = QLaunch<FMT, SR>::NW;
   const int64_t tiles = ((R + 63) / 64) * ((C + TC - 1) / TC);
-  int64_t grid = (tiles + kQWarps - 1) / kQWarps;
+  int64_t grid = (tiles + NW - 1) / NW;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), kQWarps * 32, kQSmem, st>>>(tin, trow, tcol, a);
+  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), NW * 32, QSmem<T, FMT, SR>::kTotal, st>>>(tin, trow, tcol,
+                                                                                                   a);
   count_launch();
   return launch_status();
 }
