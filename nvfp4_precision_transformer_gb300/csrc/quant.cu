@@ -76,28 +76,23 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Stochastic rounding of v to E2M1, branch-free: the magnitude moves up to the
-// next E2M1 value iff r16 * 2^-16 < (|v| - lo) / (hi - lo); |v| >= 6 saturates.
-// With a = |v| = 2^e (1 + M 2^-23), the fraction is exact in integers:
-//   a >= 1       : lo keeps the top mantissa bit, frac = (M mod 2^22) / 2^22
-//   a in [0.5, 1): lo = 0.5, frac = M / 2^23
-//   a < 0.5      : lo = 0, frac = 2a, compared as r16 < a * 2^17 (both exact in fp32)
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-  const uint32_t bits = __float_as_uint(v);
-  const uint32_t u = bits & 0x7FFFFFFFu;
-  const uint32_t sign = (bits >> 28) & 8u;
-  const uint32_t ef = u >> 23;
-  const bool ge1 = ef >= 127u;
-  const bool half = ef == 126u;
-  const uint32_t D = ge1 ? (u & 0x3FFFFFu) : (u & 0x7FFFFFu);
-  const uint32_t Rs = ge1 ? (r16 << 6) : (r16 << 7);
-  const bool up_frac = Rs < D;
-  const bool up_small = __uint2float_rn(r16) < __fmul_rn(__uint_as_float(u), 131072.0f);
-  const uint32_t lo_code = ge1 ? (((ef - 126u) << 1) | ((u >> 22) & 1u)) : (half ? 1u : 0u);
-  const bool up = (ge1 || half) ? up_frac : up_small;
-  uint32_t code = lo_code + (up ? 1u : 0u);
-  code = (u >= 0x40C00000u) ? 7u : code;  // |v| >= 6
-  return sign | code;
+// Stochastic rounding of v to the E2M1 grid, returned as a value on the grid (the
+// caller encodes it with the saturating round-to-nearest conversion, which is exact
+// there and maps anything >= 6 to 6).  With a = |v| and q the grid spacing at a
+// (0.5 below 2, 1 below 4, 2 above), t = a / q and lo = floor(t) q are exact, so
+// frac = t - floor(t) = (|v| - lo) / (hi - lo) exactly; the magnitude rounds up iff
+// r16 * 2^-16 < frac.  Floating-point form: the work lands on the FMA pipe.
+__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r16) {
+  const float a = fabsf(v);
+  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
+  const float inv_q = lt2 ? 2.0f : (lt4 ? 1.0f : 0.5f);
+  const float q = __int_as_float(0x7F000000 - __float_as_int(inv_q));  // 1 / inv_q (powers of two)
+  const float t = __fmul_rn(a, inv_q);
+  const float fl = floorf(t);
+  const float frac = __fsub_rn(t, fl);
+  const float thr = __fmul_rn(__uint2float_rn(r16), 1.52587890625e-5f);  // r16 * 2^-16, exact
+  const float m = __fmul_rn(__fadd_rn(fl, thr < frac ? 1.0f : 0.0f), q);
+  return copysignf(m, v);
 }
 
 // ---- 16-point random Hadamard transform ----------------------------------------------------
@@ -399,9 +394,15 @@ __device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4&
     for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], r), __fmul_rn(v[9 + 2 * j], r)) << (8 * j);
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) lo |= e2m1_sr(__fmul_rn(v[k], r), rand16_of(rnd0, k)) << (4 * k);
+    for (int j = 0; j < 4; ++j)
+      lo |= cvt_e2m1x2(e2m1_sr_value(__fmul_rn(v[2 * j], r), rand16_of(rnd0, 2 * j)),
+                       e2m1_sr_value(__fmul_rn(v[2 * j + 1], r), rand16_of(rnd0, 2 * j + 1)))
+            << (8 * j);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) hi |= e2m1_sr(__fmul_rn(v[8 + k], r), rand16_of(rnd1, k)) << (4 * k);
+    for (int j = 0; j < 4; ++j)
+      hi |= cvt_e2m1x2(e2m1_sr_value(__fmul_rn(v[8 + 2 * j], r), rand16_of(rnd1, 2 * j)),
+                       e2m1_sr_value(__fmul_rn(v[9 + 2 * j], r), rand16_of(rnd1, 2 * j + 1)))
+            << (8 * j);
   }
   return make_uint2(lo, hi);
 }
