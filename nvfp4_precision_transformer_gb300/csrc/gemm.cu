@@ -93,19 +93,12 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   nt = in_group / gm;
 }
 
-// CM = CTAs per cluster along M (1 or 2).  With CM = 2 the two CTAs of a cluster
-// compute vertically adjacent tiles (same N tile): each loads its own A tile and half
-// of the shared B tile (and its half of B's scale atoms) and multicasts that half to
-// both CTAs, so every CTA still holds the full B tile while the L2 -> SM traffic per
-// CTA drops from A + B to A + B/2.  A stage is refilled only after the MMAs of both
-// CTAs have consumed it (each MMA thread commits to both CTAs' empty barriers).
-template <int KIND, int CM>
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs args) {
   using C = Cfg<KIND>;
   constexpr int kStages = C::kStages;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -124,17 +117,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // work items: (group of CM vertically adjacent tiles, N tile), shared by the cluster
-  const int m_groups = (args.m_tiles + CM - 1) / CM;
-  const int num_items = m_groups * args.n_tiles;
-  const int rank = CM == 1 ? 0 : static_cast<int>(dev::cluster_ctarank());
-  const int first_item = static_cast<int>(blockIdx.x) / CM;
-  const int item_step = static_cast<int>(gridDim.x) / CM;
+  const int num_tiles = args.m_tiles * args.n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       dev::mbar_init(&full[s], 1);
-      dev::mbar_init(&empty[s], CM);
+      dev::mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       dev::mbar_init(&acc_full[s], 1);
@@ -149,8 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) dev::tmem_alloc(tmem_slot, kTmemCols);
   dev::tc_fence_before();
-  if (CM > 1) dev::cluster_sync();  // peers' barriers are initialised before any multicast
-  else __syncthreads();
+  __syncthreads();
   dev::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -164,25 +151,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
       const uint32_t tx = C::kABytes + C::kBBytes + C::kSfaBytes;
       bool ok = true;
-      for (int item = first_item; item < num_items && ok; item += item_step) {
-        int mg, nt;
-        tile_coords(item, m_groups, args.n_tiles, mg, nt);
-        const int mt = mg * CM + rank;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
         for (int kt = 0; kt < args.k_tiles; ++kt) {
           if (!dev::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
             ok = false;
             break;
           }
           uint32_t bytes = tx;
-          // the second CTA of the last cluster may hold an M tile past the end (odd tile
-          // count): its A box is zero-filled by TMA, but its scale atoms do not exist
-          const bool a_valid = mt < args.m_tiles;
           int sfb_halves = 0;
           if (C::kBlockScaled) {
             for (int h = 0; h < 2; ++h)
               if (nt * 2 + h < args.sfb_row_atoms) ++sfb_halves;
             bytes += sfb_halves * C::kSfAtoms * 512;
-            if (!a_valid) bytes -= C::kSfaBytes;
           }
           dev::mbar_expect_tx(&full[stage], bytes);
           if (KIND == kBF16 && args.a_mn) {
@@ -193,34 +175,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             dev::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, mt * BM);
           }
-          // B: this CTA's share (all of it when CM = 1, one half when CM = 2), multicast to the cluster
           if (KIND == kBF16 && args.b_mn) {
 #pragma unroll
-            for (int h = rank * (BN / 64 / CM); h < (rank + 1) * (BN / 64 / CM); ++h) {
-              if (CM == 1)
-                dev::tma_load_2d(sB + stage * C::kBBytes + h * 8192, &tmB, &full[stage], (nt * BN + 64 * h) * 2, kt * 64);
-              else
-                dev::tma_load_2d_mc(sB + stage * C::kBBytes + h * 8192, &tmB, &full[stage], (nt * BN + 64 * h) * 2,
-                                    kt * 64, kMask);
-            }
+            for (int h = 0; h < BN / 64; ++h)
+              dev::tma_load_2d(sB + stage * C::kBBytes + h * 8192, &tmB, &full[stage], (nt * BN + 64 * h) * 2, kt * 64);
           } else {
-            uint8_t* dst = sB + stage * C::kBBytes + rank * (C::kBBytes / CM);
-            if (CM == 1) dev::tma_load_2d(dst, &tmB, &full[stage], kt * 128, nt * BN);
-            else dev::tma_load_2d_mc(dst, &tmB, &full[stage], kt * 128, nt * BN + rank * (BN / CM), kMask);
+            dev::tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, nt * BN);
           }
           if (C::kBlockScaled) {
             const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
-            if (a_valid)
-              dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
-                             C::kSfaBytes, &full[stage]);
-            for (int h = rank * (2 / CM); h < (rank + 1) * (2 / CM); ++h) {
+            dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
+                           C::kSfaBytes, &full[stage]);
+            for (int h = 0; h < 2; ++h) {
               const int ra = nt * 2 + h;
-              if (ra < args.sfb_row_atoms) {
-                uint8_t* dst = sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512;
-                const uint8_t* src = args.sfb + (ra * args.sf_katoms + katom) * 512;
-                if (CM == 1) dev::bulk_load(dst, src, C::kSfAtoms * 512, &full[stage]);
-                else dev::bulk_load_mc(dst, src, C::kSfAtoms * 512, &full[stage], kMask);
-              }
+              if (ra < args.sfb_row_atoms)
+                dev::bulk_load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512,
+                               args.sfb + (ra * args.sf_katoms + katom) * 512, C::kSfAtoms * 512, &full[stage]);
             }
           }
           issued[stage] = true;
@@ -258,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
         }
       };
-      for (int item = first_item; item < num_items && ok; item += item_step, ++it) {
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
         if (!dev::mbar_wait(&acc_empty[as], aphase ^ 1u, abort_flag, args.err)) {
@@ -303,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dev::mma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_t + 8 * ks, acc);
             }
           }
-          if (CM == 1) dev::tc_commit(&empty[stage]);
-          else dev::tc_commit_mc(&empty[stage], kMask);  // the stage is shared with the peer CTA
+          dev::tc_commit(&empty[stage]);
           stage = nstage;
           phase = nphase;
         }
@@ -323,10 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = smem + C::kSmemStage + (warp - 2) * 2048;
     const float alpha = (args.alpha_a ? __ldg(args.alpha_a) : 1.0f) * (args.alpha_b ? __ldg(args.alpha_b) : 1.0f);
     int it = 0;
-    for (int item = first_item; item < num_items; item += item_step, ++it) {
-      int mg, nt;
-      tile_coords(item, m_groups, args.n_tiles, mg, nt);
-      const int mt = mg * CM + rank;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      int mt, nt;
+      tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
       const int as = it % C::kAccStages;
       const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
       if (!dev::mbar_wait(&acc_full[as], aphase, abort_flag, args.err)) break;
@@ -403,10 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) dev::bulk_wait0();
   }
 
-  __syncwarp();
   dev::tc_fence_before();
-  if (CM > 1) dev::cluster_sync();  // no CTA leaves while its peer may still signal its barriers
-  else __syncthreads();
+  __syncthreads();
   dev::tc_fence_after();
   if (warp == 1) dev::tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -428,49 +394,27 @@ uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt) {
   return d;
 }
 
-// CTAs per cluster along M for every GEMM launch (see gemm_kernel).
-constexpr int kClusterM = 2;
-
-template <int KIND, int CM>
-te_status launch_gemm_cm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
-                         int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
-                         te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
-                         int a_mn, int b_mn) {
+template <int KIND>
+te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
+                      int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
+                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
+                      int a_mn = 0, int b_mn = 0) {
   using C = Cfg<KIND>;
   static bool attr_set[64] = {false};
-  static int max_clusters[64] = {0};
   int dev_id = 0;
   cudaGetDevice(&dev_id);
-  const bool cache = dev_id >= 0 && dev_id < 64;
-  if (!cache || !attr_set[dev_id]) {
-    if (cudaFuncSetAttribute(gemm_kernel<KIND, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTotal) !=
+  if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
+    if (cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTotal) !=
         cudaSuccess)
       return record_cuda(cudaGetLastError());
-    if (CM > 1) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = CM;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.gridDim = dim3(static_cast<unsigned>(CM * (num_sms() / CM)));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = C::kSmemTotal;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, CM>, &cfg) != cudaSuccess || n < 1)
-        return record_cuda(cudaErrorInvalidConfiguration);
-      if (cache) max_clusters[dev_id] = n;
-    }
-    if (cache) attr_set[dev_id] = true;
+    attr_set[dev_id] = true;
   }
   CUtensorMap ta, tb;
   te_status s = a_mn ? make_tmap_2d(&ta, A, static_cast<uint64_t>(M) * 2, static_cast<uint64_t>(K), 64)
                      : make_tmap_2d(&ta, A, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(M), BM);
   if (s != TE_OK) return s;
   s = b_mn ? make_tmap_2d(&tb, B, static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K), 64)
-           : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN / CM);
+           : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
   if (s != TE_OK) return s;
   CUtensorMap td;
   const uint32_t esize = out == TE_F32 ? 4u : 2u;
@@ -498,39 +442,11 @@ te_status launch_gemm_cm(const void* A, const void* B, int64_t row_bytes, const 
   g.a_mn = a_mn;
   g.b_mn = b_mn;
   g.err = err;
-  const int items = ((g.m_tiles + CM - 1) / CM) * g.n_tiles;
-  if (CM == 1) {
-    const int grid = items < num_sms() ? items : num_sms();
-    gemm_kernel<KIND, CM><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, td, g);
-  } else {
-    const int avail = cache ? max_clusters[dev_id] : num_sms() / CM;
-    const int clusters = items < avail ? items : avail;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CM;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(CM * clusters));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemTotal;
-    cfg.stream = st;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CM>, ta, tb, td, g) != cudaSuccess)
-      return record_cuda(cudaGetLastError());
-  }
+  const int tiles = g.m_tiles * g.n_tiles;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_kernel<KIND><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, td, g);
   count_launch();
   return launch_status();
-}
-
-template <int KIND>
-te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
-                      int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
-                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
-                      int a_mn = 0, int b_mn = 0) {
-  return launch_gemm_cm<KIND, kClusterM>(A, B, row_bytes, sfa, sfb, sf_katoms, alpha_a, alpha_b, bias, D, out, M, N, K,
-                                        afmt, bfmt, st, a_mn, b_mn);
 }
 
 te_status check_gemm(const void* A, const void* B, const void* D, te_dtype out, int64_t M, int64_t N, int64_t K,
