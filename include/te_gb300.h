@@ -241,6 +241,12 @@ const char* te_status_str(te_status s);
  * recorded by a kernel (TE_ERR_TIMEOUT) or by the CUDA runtime (TE_ERR_CUDA). */
 te_status te_get_last_error(void);
 
+/* Self-test of the device-side failure detection: launches one warp that waits on
+ * a barrier nothing will complete; the bounded wait gives up after ~10 ms and the
+ * kernel returns, leaving TE_ERR_TIMEOUT for the next te_get_last_error().  The
+ * context stays usable (no trap, no fault). */
+te_status te_selftest_wait_timeout(void* stream);
+
 /* Number of kernels launched by this library since load (a counter the host
  * increments at every launch; for accounting in benchmarks). */
 uint64_t te_launch_count(void);

@@ -53,6 +53,7 @@ SIGNATURES = {
     "te_status_str": (ctypes.c_char_p, [_int]),
     "te_get_last_error": (_st, []),
     "te_launch_count": (_u64, []),
+    "te_selftest_wait_timeout": (_st, [_vp]),
 }
 
 
@@ -219,3 +220,7 @@ def te_get_last_error() -> int:
 
 def te_launch_count() -> int:
     return int(lib().te_launch_count())
+
+
+def te_selftest_wait_timeout(stream=None):
+    _check("te_selftest_wait_timeout", lib().te_selftest_wait_timeout(_stream(stream)))

@@ -90,22 +90,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar`, giving up after ~2 s (at 2 GHz) or when
+// Waits for phase `parity` of `bar`, giving up after `limit` SM clock cycles or when
 // another role of the CTA has already given up (*abort != 0).  On timeout the
 // device error word *err gets TE_ERR_TIMEOUT and *abort is raised.
-constexpr long long kWaitLimitCycles = 4000000000LL;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       set_error(err, kErrTimeout);
       *abort = 1;
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  return mbar_wait_limit(bar, parity, abort, err, kWaitLimitCycles);
 }
 
 // ---- TMA / bulk copies ------------------------------------------------------------------

@@ -27,6 +27,21 @@ int current_device() {
   return (d >= 0 && d < kMaxDevices) ? d : 0;
 }
 
+// One warp waits on a barrier that nothing completes: the bounded wait gives up
+// after ~10 ms, records TE_ERR_TIMEOUT and the kernel returns normally.
+__global__ void selftest_wait_kernel(int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    te::dev::mbar_init(&bar, 1);
+    abort_flag = 0;
+    te::dev::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) te::dev::mbar_wait_limit(&bar, 0, &abort_flag, err, 20000000LL);
+  __syncwarp();
+}
+
 }  // namespace
 
 namespace te {
@@ -181,5 +196,13 @@ te_status te_get_last_error(void) {
 }
 
 uint64_t te_launch_count(void) { return g_launches.load(); }
+
+te_status te_selftest_wait_timeout(void* stream) {
+  int* err = te::device_error_word();
+  if (err == nullptr) return te::record_cuda(cudaErrorInvalidDevice);
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+  te::count_launch();
+  return te::launch_status();
+}
 
 }  // extern "C"
