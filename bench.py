@@ -156,6 +156,28 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ---- DRAM traffic of the dominant kernel (from a committed ncu summary) ---------------------------
+
+def fp8_gemm_traffic():
+    """DRAM bytes per FP8 GEMM launch measured by ncu for the current gemm.cu, else None.
+
+    The summary records the sha256 prefix of the source it was measured on; a
+    changed kernel reports no traffic until it is measured again."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "gemm_fp8_dram_traffic_codonfm_layer.md")
+    csrc = os.path.join(ROOT, "nvfp4_precision_transformer_gb300", "csrc")
+    try:
+        fields = dict(line.split(":", 1) for line in open(prof) if line.count(":") == 1 and not line.startswith(("-", "#", " ")))
+        h = hashlib.sha256()
+        for name in ("gemm.cu", "common.cuh"):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+        if fields.get("kernel_source_sha256_prefix", "").strip() != h.hexdigest()[:16]:
+            return None, None
+        return int(fields["traffic_bytes_per_launch"]), int(fields["algorithmic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None, None
+
+
 # ---- CPU oracle baseline ---------------------------------------------------------------------------
 
 def oracle_sample(tokens_sample: int, hidden: int, cfg_tokens: int, layer_flops: float, layer_elems: float):
@@ -329,9 +351,11 @@ def main():
     hd = agg.get(HEADLINE) or next(iter(agg.values()))
     fp8_peak = pk["bf16_tflops_sustained"] * PEAK_RATIO["fp8"]
     achieved = hd["gemm_flops"] / (hd["gemm_ms"] * 1e-3) / 1e12
+    traffic, alg_bytes = fp8_gemm_traffic()
     roofline = {"kernel": "gemm_kernel<FP8> (tcgen05 kind::f8f6f4)", "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "traffic": None,
+                "traffic": traffic, "algorithmic_bytes": alg_bytes,
+                "flops_per_launch": round(hd["gemm_flops"] / (12 * args.steps)),
                 "peak_note": f"{pk['source']} bf16 sustained {pk['bf16_tflops_sustained']} x 2 (nominal FP8/BF16 ratio)",
                 "launches_per_layer": 12}
 
