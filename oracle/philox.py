@@ -47,19 +47,20 @@ def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):
     return tuple(v.astype(np.uint32) for v in (x0, x1, x2, x3))
 
 
-def element_rand16(n_elems: int, first: int, seed: int, copy_id: int, offset: int) -> np.ndarray:
-    """Random 16-bit value for elements ``first .. first + n_elems - 1`` of a tensor copy.
+def element_words(n_elems: int, first: int, seed: int, copy_id: int, offset: int) -> np.ndarray:
+    """32-bit random word of elements ``first .. first + n_elems - 1`` of a tensor copy.
 
-    One Philox4x32-10 output (128 bits) serves 8 consecutive elements: element g
-    (row-major index within the quantized copy) takes the 16-bit half g % 2
-    (low half first) of word (g // 2) % 4 of Philox4x32-10 with counter
-    (g // 8, copy_id, offset_lo, offset_hi) and key (seed_lo, seed_hi).
+    Elements are taken in groups of four consecutive indices; one Philox4x32-10
+    output (128 bits) serves four groups (16 elements): element g (row-major index
+    within the quantized copy) reads word (g // 4) % 4 of Philox4x32-10 with
+    counter (g // 16, copy_id, offset_lo, offset_hi) and key (seed_lo, seed_hi).
+    The four elements of a group see the same word; how they split it is part of
+    the rounding rule (oracle.quantize.sr_rand16).
     """
     g = np.arange(first, first + n_elems, dtype=np.int64)
-    grp = g >> 3
+    grp = g >> 4
     uniq = np.unique(grp)
     w = philox4x32_10(uniq & _MASK, np.uint64(copy_id), np.uint64(offset & _MASK),
                       np.uint64((offset >> 32) & _MASK), seed & _MASK, (seed >> 32) & _MASK)
     table = np.stack(w, axis=1)  # [n_groups, 4]
-    word = table[grp - uniq[0], (g >> 1) & 3]
-    return ((word >> ((g & 1) * 16).astype(np.uint32)) & 0xFFFF).astype(np.uint32)
+    return table[grp - uniq[0], (g >> 2) & 3].astype(np.uint32)
