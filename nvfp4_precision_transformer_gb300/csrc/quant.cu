@@ -76,23 +76,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Stochastic rounding of v to the E2M1 grid, returned as a value on the grid (the
-// caller encodes it with the saturating round-to-nearest conversion, which is exact
-// there and maps anything >= 6 to 6).  With a = |v| and q the grid spacing at a
-// (0.5 below 2, 1 below 4, 2 above), t = a / q and lo = floor(t) q are exact, so
-// frac = t - floor(t) = (|v| - lo) / (hi - lo) exactly; the magnitude rounds up iff
-// r16 * 2^-16 < frac.  Floating-point form: the work lands on the FMA pipe.
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r16) {
-  const float a = fabsf(v);
-  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
-  const float inv_q = lt2 ? 2.0f : (lt4 ? 1.0f : 0.5f);
-  const float q = __int_as_float(0x7F000000 - __float_as_int(inv_q));  // 1 / inv_q (powers of two)
-  const float t = __fmul_rn(a, inv_q);
-  const float fl = floorf(t);
-  const float frac = __fsub_rn(t, fl);
-  const float thr = __fmul_rn(__uint2float_rn(r16), 1.52587890625e-5f);  // r16 * 2^-16, exact
-  const float m = __fmul_rn(__fadd_rn(fl, thr < frac ? 1.0f : 0.0f), q);
-  return copysignf(m, v);
+// Four E2M1 codes with stochastic rounding (element i in bits 4i..4i+3).  The
+// hardware conversion adds 16 random bits below the kept bit and truncates; the
+// 32-bit word w feeds all four: P = (w[23:16] << 8) | w[7:0] drives elements 0
+// (as is) and 1 (bit-reversed), Q = (w[31:24] << 8) | w[15:8] elements 2 and 3.
+__device__ __forceinline__ uint32_t cvt_e2m1x4_rs(float e0, float e1, float e2, float e3, uint32_t w) {
+  uint16_t d;
+  asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;" : "=h"(d) : "f"(e3), "f"(e2), "f"(e1), "f"(e0), "r"(w));
+  return d;
 }
 
 // ---- 16-point random Hadamard transform ----------------------------------------------------
@@ -309,10 +300,6 @@ __device__ __forceinline__ float nv_senc(float A) {
 __device__ __forceinline__ uint32_t nv_scale_code(float bm, float senc) {
   return cvt_e4m3x2(__fmul_rn(__fdiv_rn(bm, 6.0f), senc), 0.0f) & 0x7Fu;
 }
-__device__ __forceinline__ uint32_t rand16_of(const uint4& w, int k) {  // k-th of the 8 values of one output
-  const uint32_t word = k < 2 ? w.x : (k < 4 ? w.y : (k < 6 ? w.z : w.w));
-  return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
-}
 
 // ---- warp-tile quantizers (FP8, MXFP8, NVFP4) ------------------------------------------------------
 // Persistent CTAs of 8 warps; every warp owns a private 2-stage ring of 64-row x
@@ -382,10 +369,10 @@ __device__ __forceinline__ uint4 fp8_pack16(const float* v, float s) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// 16 NVFP4 elements with their block's scale multiplier r; rnd0/rnd1 carry the
-// 16-bit random values of elements 0..7 / 8..15 (stochastic rounding).
+// 16 NVFP4 elements with their block's scale multiplier r; with stochastic
+// rounding, word i of `rnd` (one Philox output) drives elements 4i..4i+3.
 template <bool SR>
-__device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4& rnd0, const uint4& rnd1) {
+__device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4& rnd) {
   uint32_t lo = 0, hi = 0;
   if (!SR) {
 #pragma unroll
@@ -393,22 +380,21 @@ __device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4&
 #pragma unroll
     for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], r), __fmul_rn(v[9 + 2 * j], r)) << (8 * j);
   } else {
+    const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+    uint32_t q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      lo |= cvt_e2m1x2(e2m1_sr_value(__fmul_rn(v[2 * j], r), rand16_of(rnd0, 2 * j)),
-                       e2m1_sr_value(__fmul_rn(v[2 * j + 1], r), rand16_of(rnd0, 2 * j + 1)))
-            << (8 * j);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      hi |= cvt_e2m1x2(e2m1_sr_value(__fmul_rn(v[8 + 2 * j], r), rand16_of(rnd1, 2 * j)),
-                       e2m1_sr_value(__fmul_rn(v[9 + 2 * j], r), rand16_of(rnd1, 2 * j + 1)))
-            << (8 * j);
+    for (int i = 0; i < 4; ++i)
+      q[i] = cvt_e2m1x4_rs(__fmul_rn(v[4 * i], r), __fmul_rn(v[4 * i + 1], r), __fmul_rn(v[4 * i + 2], r),
+                           __fmul_rn(v[4 * i + 3], r), w[i]);
+    lo = q[0] | (q[1] << 16);
+    hi = q[2] | (q[3] << 16);
   }
   return make_uint2(lo, hi);
 }
 
+// Random words of the 16 elements g .. g + 15 (g a multiple of 16) of copy `copy_id`.
 __device__ __forceinline__ uint4 nv_rand(const TileArgs& a, uint64_t g, uint32_t copy_id) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(g >> 3), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(g >> 4), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
 }
 
 template <int L>
@@ -512,12 +498,9 @@ __device__ __forceinline__ void row_pass(const uint8_t* tile, uint8_t* box, int6
       for (int j = 0; j < NB16; ++j) {
         const uint32_t sc = nv_scale_code(bmax[j], senc);
         codes[h] |= sc << (8 * j);
-        uint4 rnd0 = make_uint4(0, 0, 0, 0), rnd1 = rnd0;
-        if (SR) {
-          rnd0 = nv_rand(a, g + 16 * j, 0u);
-          rnd1 = nv_rand(a, g + 16 * j + 8, 0u);
-        }
-        q[j] = nv_pack16<SR>(v[j], rtab[sc], rnd0, rnd1);
+        uint4 rnd = make_uint4(0, 0, 0, 0);
+        if (SR) rnd = nv_rand(a, g + 16 * j, 0u);
+        q[j] = nv_pack16<SR>(v[j], rtab[sc], rnd);
       }
 #pragma unroll
       for (int j = 0; j < NB16; j += 2)
@@ -607,14 +590,11 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
         }
         const uint32_t sc = nv_scale_code(m, senc);
         codes[q] |= sc << (8 * b);
-        uint4 r0v = make_uint4(0, 0, 0, 0), r1v = r0v;
-        if (SR) {
-          const uint64_t g = static_cast<uint64_t>(c0 + cl) * static_cast<uint64_t>(a.R) +
-                             static_cast<uint64_t>(r0 + b * 16);
-          r0v = nv_rand(a, g, 1u);
-          r1v = nv_rand(a, g + 8, 1u);
-        }
-        const uint2 qv = nv_pack16<SR>(x, rtab[sc], r0v, r1v);
+        uint4 rnd = make_uint4(0, 0, 0, 0);
+        if (SR)
+          rnd = nv_rand(a, static_cast<uint64_t>(c0 + cl) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(r0 + b * 16),
+                        1u);
+        const uint2 qv = nv_pack16<SR>(x, rtab[sc], rnd);
         // two 16-row blocks share one 16-byte chunk of the 32-byte box row
         uint8_t* dst = reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, cl, b >> 1)) + (b & 1) * 8;
         *reinterpret_cast<uint2*>(dst) = qv;
