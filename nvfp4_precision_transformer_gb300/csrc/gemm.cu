@@ -39,15 +39,21 @@ constexpr int BN = 256;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kGroupM = 8;
-constexpr uint32_t kTmemCols = 512;
 
-template <int KIND>
+// CG = 1: one CTA per 128 x 256 tile.  CG = 2 (BF16 / FP8): a CTA pair per 256 x 256
+// tile with the pair-wide MMA (tcgen05 cta_group::2): each CTA holds 128 rows of A
+// and 128 rows of B, the leader's single thread issues M = 256 MMAs that read both
+// CTAs' shared memory and write each CTA's own 128 accumulator rows in its TMEM.
+template <int KIND, int CG = 1>
 struct Cfg {
-  static constexpr int kStages = KIND == kNVFP4 ? 3 : 4;
+  static constexpr bool kPair = CG == 2;
+  static constexpr int kBRows = BN / CG;                      // B rows staged by one CTA
+  static constexpr int kStages = kPair ? 6 : (KIND == kNVFP4 ? 3 : 4);
   static constexpr bool kBlockScaled = KIND >= kMXFP8;
-  static constexpr int kAccStages = kBlockScaled ? 1 : 2;
+  static constexpr int kAccStages = (kBlockScaled || kPair) ? 1 : 2;
+  static constexpr uint32_t kTmemCols = kPair ? 256u : 512u;
   static constexpr int kABytes = BM * 128;
-  static constexpr int kBBytes = BN * 128;
+  static constexpr int kBBytes = kBRows * 128;
   // scale-factor atoms (512 B = 128 rows x 4 scales) per 128 rows per k-tile
   static constexpr int kSfAtoms = KIND == kMXFP8 ? 1 : (KIND == kNVFP4 ? 4 : 0);
   static constexpr int kSfaBytes = kSfAtoms * 512;
@@ -62,6 +68,7 @@ struct Cfg {
   static constexpr int kSmemStage = kSmemSfb + kStages * kSfbBytes;      // epilogue staging, 2 KB per warp
   static constexpr int kSmemBar = kSmemStage + kEpiWarps * 2048;
   static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
+  static_assert(!kPair || !kBlockScaled, "CTA pairs serve the BF16 / FP8 kinds");
   static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemTotal <= 232448, "shared memory budget");
 };
@@ -93,11 +100,12 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   nt = in_group / gm;
 }
 
-template <int KIND>
+template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs args) {
-  using C = Cfg<KIND>;
+  using C = Cfg<KIND, CG>;
+  constexpr bool kPair = C::kPair;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
@@ -117,7 +125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = args.m_tiles * args.n_tiles;
+  const int num_tiles = args.m_tiles * args.n_tiles;   // m_tiles counts BM * CG rows
+  // CTA pairs: rank 0 (the leader) issues the MMAs; both CTAs load, drain and store.
+  const uint32_t rank = kPair ? dev::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       dev::mbar_init(&acc_full[s], 1);
-      dev::mbar_init(&acc_empty[s], kEpiWarps);
+      dev::mbar_init(&acc_empty[s], kEpiWarps * CG);
     }
     dev::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -135,11 +148,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::prefetch_tmap(&tmB);
     dev::prefetch_tmap(&tmD);
   }
-  if (warp == 1) dev::tmem_alloc(tmem_slot, kTmemCols);
+  if (kPair) dev::cluster_sync();  // the peer's barriers are initialised before anyone signals them
+  if (warp == 1) {
+    if (kPair) dev::tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    else dev::tmem_alloc(tmem_slot, C::kTmemCols);
+  }
   dev::tc_fence_before();
   __syncthreads();
+  if (kPair) dev::cluster_sync();
   dev::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (kPair && !leader && threadIdx.x == 0) {
+    // the pair-wide allocation hands both CTAs the same columns; anything else is unusable
+    if (dev::ld_shared_cluster_u32(dev::mapa_shared(dev::smem_u32(tmem_slot), 0)) != tmem_base) {
+      dev::set_error(args.err, TE_ERR_UNSUPPORTED);
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -149,13 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued_phase[kStages];
       bool issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-      const uint32_t tx = C::kABytes + C::kBBytes + C::kSfaBytes;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      // pairs: the leader's full barrier counts both CTAs' bytes
+      const uint32_t tx = (C::kABytes + C::kBBytes) * CG + C::kSfaBytes;
+      bool ok = !*abort_flag;
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
         int mt, nt;
         tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
         for (int kt = 0; kt < args.k_tiles; ++kt) {
-          if (!dev::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
+          if (!dev::mbar_wait<kPair>(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
             ok = false;
             break;
           }
@@ -166,21 +193,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (nt * 2 + h < args.sfb_row_atoms) ++sfb_halves;
             bytes += sfb_halves * C::kSfAtoms * 512;
           }
-          dev::mbar_expect_tx(&full[stage], bytes);
+          if (leader) dev::mbar_expect_tx(&full[stage], bytes);
+          const int arow = (mt * CG + static_cast<int>(rank)) * BM;         // this CTA's A rows
+          const int brow = nt * BN + static_cast<int>(rank) * C::kBRows;    // this CTA's B rows
+          const uint32_t full_c = dev::mapa_shared(dev::smem_u32(&full[stage]), 0);
+          auto load = [&](uint8_t* dst, const CUtensorMap* map, int x, int y) {
+            if (kPair) dev::tma_load_2d_pair(dst, map, full_c, x, y);
+            else dev::tma_load_2d(dst, map, &full[stage], x, y);
+          };
           if (KIND == kBF16 && args.a_mn) {
             // [K, M] storage: 64 K-rows x 64 M-elements (128 B) per box, two boxes along M
 #pragma unroll
-            for (int h = 0; h < BM / 64; ++h)
-              dev::tma_load_2d(sA + stage * C::kABytes + h * 8192, &tmA, &full[stage], (mt * BM + 64 * h) * 2, kt * 64);
+            for (int h = 0; h < BM / 64; ++h) load(sA + stage * C::kABytes + h * 8192, &tmA, (arow + 64 * h) * 2, kt * 64);
           } else {
-            dev::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, mt * BM);
+            load(sA + stage * C::kABytes, &tmA, kt * 128, arow);
           }
           if (KIND == kBF16 && args.b_mn) {
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h)
-              dev::tma_load_2d(sB + stage * C::kBBytes + h * 8192, &tmB, &full[stage], (nt * BN + 64 * h) * 2, kt * 64);
+            for (int h = 0; h < C::kBRows / 64; ++h)
+              load(sB + stage * C::kBBytes + h * 8192, &tmB, (brow + 64 * h) * 2, kt * 64);
           } else {
-            dev::tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, nt * BN);
+            load(sB + stage * C::kBBytes, &tmB, kt * 128, brow);
           }
           if (C::kBlockScaled) {
             const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
@@ -198,20 +231,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) stage = 0, phase ^= 1u;
         }
       }
-      if (!ok) {
-        // Bounded wait for our own copies still in flight before the CTA exits.
+      if (!ok && leader) {
+        // Bounded wait for copies still in flight before the CTA exits (a pair's leader
+        // barrier also counts the peer's copies; the peer cannot leave before the
+        // leader, whose exit waits on the final cluster barrier).
         volatile int dummy = 0;
         for (int s = 0; s < kStages; ++s)
           if (issued[s]) dev::mbar_wait(&full[s], issued_phase[s], &dummy, args.err);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (one thread)
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (one thread; the pair's leader)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      bool ok = true;
+      bool ok = !*abort_flag;
+      auto commit = [&](uint64_t* bar, uint16_t mask) {
+        if (kPair) dev::tc_commit_pair(bar, mask);
+        else dev::tc_commit(bar);
+      };
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
@@ -228,17 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
         }
       };
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
-        if (!dev::mbar_wait(&acc_empty[as], aphase ^ 1u, abort_flag, args.err)) {
+        if (!dev::mbar_wait<kPair>(&acc_empty[as], aphase ^ 1u, abort_flag, args.err)) {
           ok = false;
           break;
         }
         dev::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
         for (int kt = 0; kt < args.k_tiles; ++kt) {
-          if (!dev::mbar_wait(&full[stage], phase, abort_flag, args.err)) {
+          if (!dev::mbar_wait<kPair>(&full[stage], phase, abort_flag, args.err)) {
             ok = false;
             break;
           }
@@ -262,9 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                 : dev::smem_desc(b_addr + 32 * ks, 0, 1024, 2);
             const uint32_t acc = (kt | ks) != 0;
             if (KIND == kBF16) {
-              dev::mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
+              if (kPair) dev::mma_f16_pair(d_tmem, adesc, bdesc, args.idesc, acc);
+              else dev::mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
             } else if (KIND == kFP8) {
-              dev::mma_f8f6f4(d_tmem, adesc, bdesc, args.idesc, acc);
+              if (kPair) dev::mma_f8f6f4_pair(d_tmem, adesc, bdesc, args.idesc, acc);
+              else dev::mma_f8f6f4(d_tmem, adesc, bdesc, args.idesc, acc);
             } else if (KIND == kMXFP8) {
               // scale byte `ks` of each 32-bit scale column (bits 29-30: A, bits 4-5: B)
               const uint32_t idesc = args.idesc | (static_cast<uint32_t>(ks) << 29) | (static_cast<uint32_t>(ks) << 4);
@@ -273,15 +314,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               dev::mma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_t + 8 * ks, acc);
             }
           }
-          dev::tc_commit(&empty[stage]);
+          commit(&empty[stage], 3);   // frees the stage in both CTAs of a pair
           stage = nstage;
           phase = nphase;
         }
         if (!ok) break;
-        dev::tc_commit(&acc_full[as]);
+        commit(&acc_full[as], 3);
       }
       // Every tcgen05 operation issued above completes before this commit fires.
-      dev::tc_commit(drain);
+      commit(drain, 1);
       volatile int dummy = 0;
       dev::mbar_wait(drain, 0, &dummy, args.err);
     }
@@ -292,12 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = smem + C::kSmemStage + (warp - 2) * 2048;
     const float alpha = (args.alpha_a ? __ldg(args.alpha_a) : 1.0f) * (args.alpha_b ? __ldg(args.alpha_b) : 1.0f);
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    const uint32_t acc_empty_c = dev::mapa_shared(dev::smem_u32(&acc_empty[0]), 0);  // the leader's
+    for (int tile = unit; tile < num_tiles; tile += units, ++it) {
       int mt, nt;
       tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
       const int as = it % C::kAccStages;
       const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
-      if (!dev::mbar_wait(&acc_full[as], aphase, abort_flag, args.err)) break;
+      if (!dev::mbar_wait<kPair>(&acc_full[as], aphase, abort_flag, args.err)) break;
       dev::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(as * BN + half * 128);
@@ -309,11 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) dev::reg_fence(acc[c]);
       dev::tc_fence_before();
       __syncwarp();
-      if (lane == 0) dev::mbar_arrive(&acc_empty[as]);
+      if (lane == 0) {
+        if (kPair) dev::mbar_arrive_cluster(acc_empty_c + static_cast<uint32_t>(as * 8));
+        else dev::mbar_arrive(&acc_empty[as]);
+      }
 
       // Stage 32 rows x 64 bytes at a time in this warp's shared-memory box and write it
       // with a TMA store (the store clips rows >= M and columns >= N).
-      const int m0 = mt * BM + quarter * 32;
+      const int m0 = (mt * CG + static_cast<int>(rank)) * BM + quarter * 32;
       const int n0 = nt * BN + half * 128;
       // One 32-row x 64-byte box: lane-row words w[0..15] -> staging buffer -> TMA store.
       auto store_box = [&](const uint32_t (&w)[16], int nb) {
@@ -373,8 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   dev::tc_fence_before();
   __syncthreads();
+  if (kPair) dev::cluster_sync();  // the leader's MMAs read the peer's shared memory until here
   dev::tc_fence_after();
-  if (warp == 1) dev::tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (kPair) dev::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else dev::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
 }
 
 // ---- host launch ----------------------------------------------------------------------------------
@@ -383,30 +432,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 // non-block-scaled kinds, A / B formats in bits 7-9 / 10-12, K-major operands
 // (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28; for the
 // block-scaled kinds bit 23 selects the scale format (UE8M0 = 1, UE4M3 = 0).
-uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt) {
+uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt, int m) {
   uint32_t d = 0;
   if (kind == kBF16 || kind == kFP8) d |= 1u << 4;
   d |= (afmt & 7u) << 7;
   d |= (bfmt & 7u) << 10;
   d |= static_cast<uint32_t>(BN >> 3) << 17;
   if (kind == kMXFP8) d |= 1u << 23;
-  d |= static_cast<uint32_t>(BM >> 4) << 24;
+  d |= static_cast<uint32_t>(m >> 4) << 24;
   return d;
 }
 
-template <int KIND>
+template <int KIND, int CG = 1>
 te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
                       int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
                       te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
                       int a_mn = 0, int b_mn = 0) {
-  using C = Cfg<KIND>;
+  using C = Cfg<KIND, CG>;
   static bool attr_set[64] = {false};
+  static int max_clusters[64] = {0};
   int dev_id = 0;
   cudaGetDevice(&dev_id);
-  if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
-    if (cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTotal) !=
+  if (dev_id < 0 || dev_id >= 64) return TE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemTotal;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!attr_set[dev_id]) {
+    if (cudaFuncSetAttribute(gemm_kernel<KIND, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTotal) !=
         cudaSuccess)
       return record_cuda(cudaGetLastError());
+    int n = num_sms() / CG;
+    if (CG > 1) {
+      // clusters that can be resident at once (a GPC may leave an SM unpaired)
+      cfg.gridDim = dim3(CG * n, 1, 1);
+      int mc = 0;
+      if (cudaOccupancyMaxActiveClusters(&mc, gemm_kernel<KIND, CG>, &cfg) != cudaSuccess || mc <= 0)
+        return record_cuda(cudaGetLastError());
+      n = mc < n ? mc : n;
+    }
+    max_clusters[dev_id] = n;
     attr_set[dev_id] = true;
   }
   CUtensorMap ta, tb;
@@ -414,7 +486,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
                      : make_tmap_2d(&ta, A, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(M), BM);
   if (s != TE_OK) return s;
   s = b_mn ? make_tmap_2d(&tb, B, static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K), 64)
-           : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), BN);
+           : make_tmap_2d(&tb, B, static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(N), C::kBRows);
   if (s != TE_OK) return s;
   CUtensorMap td;
   const uint32_t esize = out == TE_F32 ? 4u : 2u;
@@ -427,7 +499,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.N = static_cast<int>(N);
   g.K = static_cast<int>(K);
   g.k_tiles = static_cast<int>((row_bytes + 127) / 128);
-  g.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  g.m_tiles = static_cast<int>((M + BM * CG - 1) / (BM * CG));
   g.n_tiles = static_cast<int>((N + BN - 1) / BN);
   g.sfa = sfa;
   g.sfb = sfb;
@@ -438,13 +510,15 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.bias = bias;
   g.D = D;
   g.out_f32 = out == TE_F32;
-  g.idesc = make_idesc(KIND, afmt, bfmt) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
+  g.idesc = make_idesc(KIND, afmt, bfmt, BM * CG) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
   g.a_mn = a_mn;
   g.b_mn = b_mn;
   g.err = err;
   const int tiles = g.m_tiles * g.n_tiles;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<KIND><<<grid, kThreads, C::kSmemTotal, st>>>(ta, tb, td, g);
+  const int units = tiles < max_clusters[dev_id] ? tiles : max_clusters[dev_id];
+  cfg.gridDim = dim3(static_cast<unsigned>(CG * units), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, ta, tb, td, g) != cudaSuccess)
+    return record_cuda(cudaGetLastError());
   count_launch();
   return launch_status();
 }
@@ -476,7 +550,7 @@ te_status te_gemm_bf16(const void* A, te_layout a_layout, const void* B, te_layo
     return TE_ERR_ARG;
   te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
   if (s != TE_OK || M * N == 0) return s;
-  return launch_gemm<kBF16>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, M, N, K, 1u, 1u,
+  return launch_gemm<kBF16, 2>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, M, N, K, 1u, 1u,
                             static_cast<cudaStream_t>(stream), a_layout == TE_MN_MAJOR, b_layout == TE_MN_MAJOR);
 }
 
@@ -487,7 +561,7 @@ te_status te_gemm_fp8(const uint8_t* A, te_dtype fa, const uint8_t* B, te_dtype 
   te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
   if (s != TE_OK || M * N == 0) return s;
   if (!a_scale_inv || !b_scale_inv) return TE_ERR_NULL;
-  return launch_gemm<kFP8>(A, B, K, nullptr, nullptr, 0, a_scale_inv, b_scale_inv, bias, D, out_dtype, M, N, K,
+  return launch_gemm<kFP8, 2>(A, B, K, nullptr, nullptr, 0, a_scale_inv, b_scale_inv, bias, D, out_dtype, M, N, K,
                            f8_code(fa), f8_code(fb), static_cast<cudaStream_t>(stream));
 }
 

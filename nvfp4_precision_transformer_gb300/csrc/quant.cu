@@ -106,6 +106,27 @@ __device__ __forceinline__ void rht16(float (&v)[16], uint32_t signs) {
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
+// ---- packed fp32 pairs (two IEEE round-to-nearest operations per instruction) ----------------
+
+__device__ __forceinline__ float2 f2neg(float2 a) { return make_float2(-a.x, -a.y); }
+// Butterflies h = 1, 2, 4, 8 of the 16-point Hadamard transform on two columns at
+// once (y[r] holds row r of both); the same operations in the same order as rht16
+// (a - b is computed as a + (-b), which is the same rounded result).
+__device__ __forceinline__ void hadamard16x2(float2 (&y)[16]) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      const float2 a = y[i], b = y[i + h];
+      y[i] = __fadd2_rn(a, b);
+      y[i + h] = __fadd2_rn(a, f2neg(b));
+    }
+  }
+}
+// Sign-flip mask of row j for a word of two bf16 values (both flipped when bit j of signs is set).
+__device__ __forceinline__ uint32_t rht_sign2(uint32_t signs, int j) { return (0u - ((signs >> j) & 1u)) & 0x80008000u; }
+
 // ---- reductions -----------------------------------------------------------------------------
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -230,24 +251,65 @@ inline unsigned patch_blocks(int64_t rows, int64_t cols, int pr, int pc) {
 template <typename T, bool RHT>
 __global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C, float* amax,
                                                            float* amax_rht, uint32_t signs) {
-  // the rotated amax transforms every column of the patch: 8-byte row vectors halve its registers
-  using P = Patch<T, RHT ? 8 : 16, 16>;
+  static_assert(!RHT, "the rotated amax has its own kernel");
+  using P = Patch<T, 16, 16>;
   P p;
   p.load(x, R, C);
   block_max_to(p.absmax(), amax);
-  if (RHT) {
-    float mr = 0.0f;
+}
+
+// Plain and rotated amax from one read.  Persistent grid: each thread walks 16-row x
+// 8-byte patches with the next patch's loads in flight while it rotates the current
+// one; columns are rotated in pairs as packed fp32 values, and the 1/4 of the
+// transform is applied to the maximum (exact: scaling by 1/4 and rounding are monotone).
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                               float* amax, float* amax_rht, uint32_t signs) {
+  constexpr int PC = 8 / sizeof(T);  // columns per patch
+  const int64_t ncg = C / PC;
+  const int64_t total = (R / 16) * ncg;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  auto load = [&](int64_t i, uint2 (&raw)[16]) {
+    if (i < total) {
+      const int64_t band = i / ncg;
+      const T* q = x + band * 16 * C + (i - band * ncg) * PC;
 #pragma unroll
-    for (int i = 0; i < P::PC; ++i) {
-      float col[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) col[r] = p.at(r, i);
-      rht16(col, signs);
-#pragma unroll
-      for (int r = 0; r < 16; ++r) mr = fmaxf(mr, fabsf(col[r]));
+      for (int r = 0; r < 16; ++r) raw[r] = __ldg(reinterpret_cast<const uint2*>(q + r * C));
     }
-    block_max_to(mr, amax_rht);
+  };
+  uint2 cur[16], nxt[16];
+  load(idx, cur);
+  float m = 0.0f, mr = 0.0f;
+  for (; idx < total; idx += stride) {
+    load(idx + stride, nxt);
+#pragma unroll
+    for (int k = 0; k < (sizeof(T) == 2 ? 2 : 1); ++k) {  // column pairs of the patch
+      float2 y[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float lo, hi;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t w = (k == 0 ? cur[r].x : cur[r].y) ^ rht_sign2(signs, r);
+          lo = __uint_as_float(w << 16);
+          hi = __uint_as_float(w & 0xFFFF0000u);
+        } else {
+          const uint32_t sg = (0u - ((signs >> r) & 1u)) & 0x80000000u;
+          lo = __uint_as_float(cur[r].x ^ sg);
+          hi = __uint_as_float(cur[r].y ^ sg);
+        }
+        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+        y[r] = make_float2(lo, hi);
+      }
+      hadamard16x2(y);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) mr = fmaxf(mr, fmaxf(fabsf(y[r].x), fabsf(y[r].y)));
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) cur[r] = nxt[r];
   }
+  block_max_to(m, amax);
+  block_max_to(__fmul_rn(mr, 0.25f), amax_rht);
 }
 
 // ---- DelayedScaling update ----------------------------------------------------------------------
@@ -369,27 +431,38 @@ __device__ __forceinline__ uint4 fp8_pack16(const float* v, float s) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// 16 NVFP4 elements with their block's scale multiplier r; with stochastic
-// rounding, word i of `rnd` (one Philox output) drives elements 4i..4i+3.
+// 16 already-scaled NVFP4 values -> 16 E2M1 codes (element i in nibble i); with
+// stochastic rounding, word i of `rnd` (one Philox output) drives elements 4i..4i+3.
 template <bool SR>
-__device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4& rnd) {
+__device__ __forceinline__ uint2 nv_encode16(const float* s, const uint4& rnd) {
   uint32_t lo = 0, hi = 0;
   if (!SR) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) lo |= cvt_e2m1x2(__fmul_rn(v[2 * j], r), __fmul_rn(v[2 * j + 1], r)) << (8 * j);
+    for (int j = 0; j < 4; ++j) lo |= cvt_e2m1x2(s[2 * j], s[2 * j + 1]) << (8 * j);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(__fmul_rn(v[8 + 2 * j], r), __fmul_rn(v[9 + 2 * j], r)) << (8 * j);
+    for (int j = 0; j < 4; ++j) hi |= cvt_e2m1x2(s[8 + 2 * j], s[9 + 2 * j]) << (8 * j);
   } else {
     const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
     uint32_t q[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      q[i] = cvt_e2m1x4_rs(__fmul_rn(v[4 * i], r), __fmul_rn(v[4 * i + 1], r), __fmul_rn(v[4 * i + 2], r),
-                           __fmul_rn(v[4 * i + 3], r), w[i]);
+    for (int i = 0; i < 4; ++i) q[i] = cvt_e2m1x4_rs(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3], w[i]);
     lo = q[0] | (q[1] << 16);
     hi = q[2] | (q[3] << 16);
   }
   return make_uint2(lo, hi);
+}
+// 16 NVFP4 elements with their block's scale multiplier r (x * r in packed pairs).
+template <bool SR>
+__device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4& rnd) {
+  const float2 rr = make_float2(r, r);
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 t = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), rr);
+    s[2 * i] = t.x;
+    s[2 * i + 1] = t.y;
+  }
+  return nv_encode16<SR>(s, rnd);
 }
 
 // Random words of the 16 elements g .. g + 15 (g a multiple of 16) of copy `copy_id`.
@@ -415,13 +488,13 @@ struct QGeom {
   static constexpr int COL_BOX = TC * COL_W;               // staging box bytes of the col copy
 };
 
-// Warps per CTA and input stages per warp.  The stochastic-rounding NVFP4 kernel is
-// arithmetic-bound (Philox + rounding per element), so it trades the second stage
-// for twice the warps; every other configuration is bandwidth-bound.
+// Warps per CTA and input stages per warp (the same for every format: with the
+// hardware stochastic-rounding conversion no variant is arithmetic-bound enough to
+// prefer more warps over a second stage).
 template <int FMT, bool SR>
 struct QLaunch {
-  static constexpr int NW = (FMT == kQNV && SR) ? 16 : 8;
-  static constexpr int NS = (FMT == kQNV && SR) ? 1 : 2;
+  static constexpr int NW = 8;
+  static constexpr int NS = 2;
 };
 template <typename T, int FMT, bool SR>
 struct QSmem {
@@ -539,65 +612,115 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
   const bool rht = FMT == kQNV && (a.flags & TE_NVFP4_RHT_COL) != 0;
   uint32_t codes[NCL] = {};
   constexpr int RB = FMT == kQMX ? 32 : 16;  // rows per block of the col copy
+  if constexpr (FMT == kQNV && NCL == 2) {
+    // NVFP4, two columns per lane: both columns travel as packed fp32 pairs
+    // through the sign flip, the Hadamard butterflies, the 1/4 and the block scaling.
 #pragma unroll 1
-  for (int b = 0; b < 64 / RB; ++b) {
-    float v[NCL][RB];
+    for (int b = 0; b < 4; ++b) {
+      float2 y[16];
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      const uint32_t w = tile_word(tile, b * RB + r, lane);
-      if constexpr (sizeof(T) == 2) {
-        v[0][r] = __uint_as_float(w << 16);
-        v[NCL - 1][r] = __uint_as_float(w & 0xFFFF0000u);
-      } else {
-        v[0][r] = __uint_as_float(w);
+      for (int r = 0; r < 16; ++r) {
+        uint32_t w = tile_word(tile, b * 16 + r, lane);
+        if (rht) w ^= rht_sign2(a.signs, r);
+        y[r] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
       }
+      if (rht) {
+        hadamard16x2(y);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) y[r] = __fmul2_rn(y[r], make_float2(0.25f, 0.25f));
+      }
+      float ma = 0.0f, mb = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        ma = fmaxf(ma, fabsf(y[r].x));
+        mb = fmaxf(mb, fabsf(y[r].y));
+      }
+      if (two_d) ma = mb = lanes_max<8>(fmaxf(ma, mb));  // 16 rows x 16 columns
+      const uint32_t sa = nv_scale_code(ma, senc), sb = nv_scale_code(mb, senc);
+      codes[0] |= sa << (8 * b);
+      codes[1] |= sb << (8 * b);
+      const float2 rr = make_float2(rtab[sa], rtab[sb]);
+      float va[16], vb[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float2 t = __fmul2_rn(y[r], rr);
+        va[r] = t.x;
+        vb[r] = t.y;
+      }
+      uint4 rnd_a = make_uint4(0, 0, 0, 0), rnd_b = rnd_a;
+      if (SR) {
+        const uint64_t g = static_cast<uint64_t>(c0 + 2 * lane) * static_cast<uint64_t>(a.R) +
+                           static_cast<uint64_t>(r0 + b * 16);
+        rnd_a = nv_rand(a, g, 1u);
+        rnd_b = nv_rand(a, g + static_cast<uint64_t>(a.R), 1u);
+      }
+      const uint2 qa = nv_encode16<SR>(va, rnd_a), qb = nv_encode16<SR>(vb, rnd_b);
+      // two 16-row blocks share one 16-byte chunk of the 32-byte box row
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, 2 * lane, b >> 1)) + (b & 1) * 8) = qa;
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, 2 * lane + 1, b >> 1)) + (b & 1) * 8) =
+          qb;
     }
-    float tile_m = 0.0f;
-    if (two_d) {
-#pragma unroll
-      for (int qq = 0; qq < NCL; ++qq)
-#pragma unroll
-        for (int r = 0; r < RB; ++r) tile_m = fmaxf(tile_m, fabsf(v[qq][r]));
-      tile_m = lanes_max<16 / NCL>(tile_m);  // 16 rows x 16 columns
-    }
-#pragma unroll
-    for (int q = 0; q < NCL; ++q) {
-      const int cl = lane * NCL + q;  // column within the tile = row of the col-copy box
-      if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
-        if (track_max)
-#pragma unroll
-          for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
-        *stage_chunk<G::COL_W>(box, cl, b) = fp8_pack16<FMT>(v[q], s_fp8);
-      } else if constexpr (FMT == kQMX) {
-        float m = 0.0f;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
-        const int E = mx_exponent(m);
-        const float mult = mx_mult(E);
-        *stage_chunk<G::COL_W>(box, cl, 2 * b) = fp8_pack16<kQE4M3>(&v[q][0], mult);
-        *stage_chunk<G::COL_W>(box, cl, 2 * b + 1) = fp8_pack16<kQE4M3>(&v[q][16], mult);
-        codes[q] |= static_cast<uint32_t>(E + 127) << (8 * b);
-      } else {
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = v[q][r];
-        if (rht) rht16(x, a.signs);
-        float m = tile_m;
-        if (!two_d) {
-          m = 0.0f;
-#pragma unroll
-          for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(x[r]));
+  } else {
+  #pragma unroll 1
+    for (int b = 0; b < 64 / RB; ++b) {
+      float v[NCL][RB];
+  #pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const uint32_t w = tile_word(tile, b * RB + r, lane);
+        if constexpr (sizeof(T) == 2) {
+          v[0][r] = __uint_as_float(w << 16);
+          v[NCL - 1][r] = __uint_as_float(w & 0xFFFF0000u);
+        } else {
+          v[0][r] = __uint_as_float(w);
         }
-        const uint32_t sc = nv_scale_code(m, senc);
-        codes[q] |= sc << (8 * b);
-        uint4 rnd = make_uint4(0, 0, 0, 0);
-        if (SR)
-          rnd = nv_rand(a, static_cast<uint64_t>(c0 + cl) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(r0 + b * 16),
-                        1u);
-        const uint2 qv = nv_pack16<SR>(x, rtab[sc], rnd);
-        // two 16-row blocks share one 16-byte chunk of the 32-byte box row
-        uint8_t* dst = reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, cl, b >> 1)) + (b & 1) * 8;
-        *reinterpret_cast<uint2*>(dst) = qv;
+      }
+      float tile_m = 0.0f;
+      if (two_d) {
+  #pragma unroll
+        for (int qq = 0; qq < NCL; ++qq)
+  #pragma unroll
+          for (int r = 0; r < RB; ++r) tile_m = fmaxf(tile_m, fabsf(v[qq][r]));
+        tile_m = lanes_max<16 / NCL>(tile_m);  // 16 rows x 16 columns
+      }
+  #pragma unroll
+      for (int q = 0; q < NCL; ++q) {
+        const int cl = lane * NCL + q;  // column within the tile = row of the col-copy box
+        if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
+          if (track_max)
+  #pragma unroll
+            for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
+          *stage_chunk<G::COL_W>(box, cl, b) = fp8_pack16<FMT>(v[q], s_fp8);
+        } else if constexpr (FMT == kQMX) {
+          float m = 0.0f;
+  #pragma unroll
+          for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
+          const int E = mx_exponent(m);
+          const float mult = mx_mult(E);
+          *stage_chunk<G::COL_W>(box, cl, 2 * b) = fp8_pack16<kQE4M3>(&v[q][0], mult);
+          *stage_chunk<G::COL_W>(box, cl, 2 * b + 1) = fp8_pack16<kQE4M3>(&v[q][16], mult);
+          codes[q] |= static_cast<uint32_t>(E + 127) << (8 * b);
+        } else {
+          float x[16];
+  #pragma unroll
+          for (int r = 0; r < 16; ++r) x[r] = v[q][r];
+          if (rht) rht16(x, a.signs);
+          float m = tile_m;
+          if (!two_d) {
+            m = 0.0f;
+  #pragma unroll
+            for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(x[r]));
+          }
+          const uint32_t sc = nv_scale_code(m, senc);
+          codes[q] |= sc << (8 * b);
+          uint4 rnd = make_uint4(0, 0, 0, 0);
+          if (SR)
+            rnd = nv_rand(a, static_cast<uint64_t>(c0 + cl) * static_cast<uint64_t>(a.R) + static_cast<uint64_t>(r0 + b * 16),
+                          1u);
+          const uint2 qv = nv_pack16<SR>(x, rtab[sc], rnd);
+          // two 16-row blocks share one 16-byte chunk of the 32-byte box row
+          uint8_t* dst = reinterpret_cast<uint8_t*>(stage_chunk<G::COL_W>(box, cl, b >> 1)) + (b & 1) * 8;
+          *reinterpret_cast<uint2*>(dst) = qv;
+        }
       }
     }
   }
@@ -738,22 +861,22 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
   if (amax_rht != nullptr && cudaMemsetAsync(amax_rht, 0, sizeof(float), st) != cudaSuccess)
     return record_cuda(cudaGetLastError());
   if (rows * cols == 0) return TE_OK;
-  if (in == TE_BF16) {
-    const auto* p = static_cast<const __nv_bfloat16*>(x);
-    if (amax_rht)
-      amax_kernel<__nv_bfloat16, true><<<patch_blocks(rows, cols, 16, 4), kThreads, 0, st>>>(p, rows, cols, amax,
-                                                                                           amax_rht, signs);
+  if (amax_rht != nullptr) {
+    const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? 4 : 2));
+    const int64_t want = (patches + kThreads - 1) / kThreads;
+    const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
+    if (in == TE_BF16)
+      amax_rht_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, amax,
+                                                                amax_rht, signs);
     else
-      amax_kernel<__nv_bfloat16, false><<<patch_blocks(rows, cols, 16, 8), kThreads, 0, st>>>(p, rows, cols, amax,
-                                                                                            nullptr, signs);
+      amax_rht_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols, amax, amax_rht,
+                                                        signs);
+  } else if (in == TE_BF16) {
+    amax_kernel<__nv_bfloat16, false><<<patch_blocks(rows, cols, 16, 8), kThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, cols, amax, nullptr, signs);
   } else {
-    const auto* p = static_cast<const float*>(x);
-    if (amax_rht)
-      amax_kernel<float, true><<<patch_blocks(rows, cols, 16, 2), kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
-                                                                                   signs);
-    else
-      amax_kernel<float, false><<<patch_blocks(rows, cols, 16, 4), kThreads, 0, st>>>(p, rows, cols, amax, nullptr,
-                                                                                    signs);
+    amax_kernel<float, false><<<patch_blocks(rows, cols, 16, 4), kThreads, 0, st>>>(static_cast<const float*>(x), rows,
+                                                                                 cols, amax, nullptr, signs);
   }
   count_launch();
   return launch_status();
