@@ -10,9 +10,9 @@
 // is a 128-byte row slice (one 128-byte-swizzle atom) and 4 instructions.
 //
 // CTA = 10 warps, one CTA per SM (the shared-memory footprint guarantees it):
-//   warp 0      TMA producer: A tile [128 x 128 B], B tile [256 x 128 B] and, for the
-//               block-scaled kinds, the scale-factor atoms (bulk copies), into a
-//               4-stage shared-memory ring guarded by full/empty mbarriers;
+//   warp 0      TMA producer: A tile [128 x 128 B], B tile and, for the block-scaled
+//               kinds, the scale-factor atoms (bulk copies), into a shared-memory
+//               ring guarded by full/empty mbarriers;
 //   warp 1      allocates TMEM and issues the MMAs from one thread: scale factors
 //               are copied smem -> TMEM with tcgen05.cp, each k-tile's MMAs are
 //               followed by tcgen05.commit onto the stage's empty barrier, each
@@ -20,6 +20,18 @@
 //   warps 2-9   epilogue: each warp owns a 32-lane quarter of TMEM and a 128-column
 //               half of the 128 x 256 accumulator, drains it to registers, releases
 //               the accumulator, then applies alpha / bias, rounds and stores.
+// BF16 and FP8 run as CTA pairs (2-CTA clusters, tcgen05 cta_group::2) on 256 x 256
+// tiles: each CTA stages 128 rows of A and 128 rows of B (6 stages), the leader's
+// thread issues M = 256 MMAs that read both CTAs' operands and write each CTA's 128
+// accumulator rows into its own TMEM, and its commits free the stage and publish the
+// accumulator in both CTAs; loads of both CTAs complete on the leader's full barrier,
+// and both CTAs' epilogue warps arrive on the leader's accumulator-empty barrier.
+// Halving each SM's share of B halves its shared-memory traffic for B.  MXFP8 and
+// NVFP4 run one CTA per 128 x 256 tile (4 / 3 stages of A [128 x 128 B] + B [256 x 128 B]):
+// their pair form (each CTA also stages the scale atoms of all 256 B rows, since each
+// half of a pair MMA reads every B row's scales from its own TMEM; scale atoms then
+// arrive by TMA so that they complete on the leader's barrier) is supported by the
+// template but measured 0-4 % slower, the per-SM scale-factor copies being unchanged.
 // The accumulator is double-buffered in TMEM for BF16/FP8 (2 x 256 columns); the
 // block-scaled kinds keep one 256-column accumulator plus a per-stage scale-factor
 // region and rely on the early release of the register drain for overlap.
@@ -48,18 +60,21 @@ template <int KIND, int CG = 1>
 struct Cfg {
   static constexpr bool kPair = CG == 2;
   static constexpr int kBRows = BN / CG;                      // B rows staged by one CTA
-  static constexpr int kStages = kPair ? 6 : (KIND == kNVFP4 ? 3 : 4);
+  static constexpr int kStages = kPair ? (KIND == kNVFP4 ? 5 : 6) : (KIND == kNVFP4 ? 3 : 4);
   static constexpr bool kBlockScaled = KIND >= kMXFP8;
-  static constexpr int kAccStages = (kBlockScaled || kPair) ? 1 : 2;
-  static constexpr uint32_t kTmemCols = kPair ? 256u : 512u;
+  static constexpr int kAccStages = kBlockScaled ? 1 : 2;
+  static constexpr uint32_t kTmemCols = 512u;
   static constexpr int kABytes = BM * 128;
   static constexpr int kBBytes = kBRows * 128;
   // scale-factor atoms (512 B = 128 rows x 4 scales) per 128 rows per k-tile
   static constexpr int kSfAtoms = KIND == kMXFP8 ? 1 : (KIND == kNVFP4 ? 4 : 0);
   static constexpr int kSfaBytes = kSfAtoms * 512;
-  static constexpr int kSfbBytes = 2 * kSfAtoms * 512;
+  // B's scale atoms of all 256 B rows per k-tile: in a pair each CTA's half of the MMA
+  // reads the scales of every B row from its own TMEM
+  static constexpr int kSfbAtoms = 2 * kSfAtoms;
+  static constexpr int kSfbBytes = kSfbAtoms * 512;
   static constexpr int kSfaCols = 4 * kSfAtoms;
-  static constexpr int kSfbCols = 8 * kSfAtoms;
+  static constexpr int kSfbCols = 4 * kSfbAtoms;
   static constexpr int kSfTmemBase = 256;
   static constexpr int kSmemA = 0;
   static constexpr int kSmemB = kSmemA + kStages * kABytes;
@@ -68,7 +83,6 @@ struct Cfg {
   static constexpr int kSmemStage = kSmemSfb + kStages * kSfbBytes;      // epilogue staging, 2 KB per warp
   static constexpr int kSmemBar = kSmemStage + kEpiWarps * 2048;
   static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
-  static_assert(!kPair || !kBlockScaled, "CTA pairs serve the BF16 / FP8 kinds");
   static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemTotal <= 232448, "shared memory budget");
 };
@@ -103,7 +117,8 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSa,
+                const __grid_constant__ CUtensorMap tmSb, const __grid_constant__ GemmArgs args) {
   using C = Cfg<KIND, CG>;
   constexpr bool kPair = C::kPair;
   constexpr int kStages = C::kStages;
@@ -176,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
       // pairs: the leader's full barrier counts both CTAs' bytes
-      const uint32_t tx = (C::kABytes + C::kBBytes) * CG + C::kSfaBytes;
+      const uint32_t tx = kPair ? (C::kABytes + C::kBBytes + C::kSfaBytes + C::kSfbBytes) * CG
+                                : C::kABytes + C::kBBytes + C::kSfaBytes;
       bool ok = !*abort_flag;
       for (int tile = unit; tile < num_tiles && ok; tile += units) {
         int mt, nt;
@@ -188,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint32_t bytes = tx;
           int sfb_halves = 0;
-          if (C::kBlockScaled) {
+          if (C::kBlockScaled && !kPair) {
             for (int h = 0; h < 2; ++h)
               if (nt * 2 + h < args.sfb_row_atoms) ++sfb_halves;
             bytes += sfb_halves * C::kSfAtoms * 512;
@@ -215,7 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             load(sB + stage * C::kBBytes, &tmB, kt * 128, brow);
           }
-          if (C::kBlockScaled) {
+          if (C::kBlockScaled && kPair) {
+            // scale atoms by TMA (completion on the leader's barrier): the scale tensor is
+            // viewed as 256-byte rows, so a 128-row group's atoms of one k-tile are
+            // 2 * kSfAtoms consecutive rows; boxes past the end are zero-filled
+            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
+            load(sSfa + stage * C::kSfaBytes, &tmSa, 0,
+                 static_cast<int>(((mt * CG + static_cast<int>(rank)) * args.sf_katoms + katom) * 2));
+            for (int h = 0; h < 2; ++h)
+              load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512, &tmSb, 0,
+                   static_cast<int>(((nt * 2 + h) * args.sf_katoms + katom) * 2));
+          } else if (C::kBlockScaled) {
             const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
             dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
                            C::kSfaBytes, &full[stage]);
@@ -258,13 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sfa_t = sf_slot(st), sfb_t = sfa_t + C::kSfaCols;
         const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
         const uint32_t sfb_s = dev::smem_u32(sSfb + st * C::kSfbBytes);
+        auto cp = [&](uint32_t t, uint32_t sa) {
+          if (kPair) dev::tc_cp_32x128b_x4_pair(t, dev::smem_desc(sa, 0, 128, 0));
+          else dev::tc_cp_32x128b_x4(t, dev::smem_desc(sa, 0, 128, 0));
+        };
 #pragma unroll
         for (int j = 0; j < C::kSfAtoms; ++j) {
-          dev::tc_cp_32x128b_x4(sfa_t + 4 * j, dev::smem_desc(sfa_s + 512 * j, 0, 128, 0));
+          cp(sfa_t + 4 * j, sfa_s + 512 * j);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            dev::tc_cp_32x128b_x4(sfb_t + 8 * j + 4 * h,
-                                  dev::smem_desc(sfb_s + h * C::kSfAtoms * 512 + 512 * j, 0, 128, 0));
+          for (int h = 0; h < 2; ++h) cp(sfb_t + 8 * j + 4 * h, sfb_s + h * C::kSfAtoms * 512 + 512 * j);
         }
       };
       for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
@@ -309,9 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (KIND == kMXFP8) {
               // scale byte `ks` of each 32-bit scale column (bits 29-30: A, bits 4-5: B)
               const uint32_t idesc = args.idesc | (static_cast<uint32_t>(ks) << 29) | (static_cast<uint32_t>(ks) << 4);
-              dev::mma_mxf8f6f4(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, acc);
+              if (kPair) dev::mma_mxf8f6f4_pair(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, acc);
+              else dev::mma_mxf8f6f4(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, acc);
             } else {
-              dev::mma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_t + 8 * ks, acc);
+              const uint32_t sfb_k = sfb_t + 8 * ks;
+              if (kPair) dev::mma_mxf4nvf4_pair(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_k, acc);
+              else dev::mma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * ks, sfb_k, acc);
             }
           }
           commit(&empty[stage], 3);   // frees the stage in both CTAs of a pair
@@ -492,6 +523,17 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   const uint32_t esize = out == TE_F32 ? 4u : 2u;
   s = make_tmap_2d_plain(&td, D, static_cast<uint64_t>(N) * esize, static_cast<uint64_t>(M), 64u, 32u);
   if (s != TE_OK) return s;
+  // scale tensors as 256-byte rows (CTA pairs load them by TMA); unused otherwise
+  CUtensorMap tsa = td, tsb = td;
+  if (C::kBlockScaled && C::kPair) {
+    const uint64_t rows_a = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>(sf_katoms) * 2;
+    const uint64_t rows_b = static_cast<uint64_t>((N + 127) / 128) * static_cast<uint64_t>(sf_katoms) * 2;
+    if (rows_a >= (uint64_t(1) << 31) || rows_b >= (uint64_t(1) << 31)) return TE_ERR_SHAPE;
+    s = make_tmap_2d_plain(&tsa, sfa, 256u, rows_a, 256u, static_cast<uint32_t>(2 * C::kSfAtoms));
+    if (s != TE_OK) return s;
+    s = make_tmap_2d_plain(&tsb, sfb, 256u, rows_b, 256u, static_cast<uint32_t>(2 * C::kSfAtoms));
+    if (s != TE_OK) return s;
+  }
   int* err = device_error_word();
   if (err == nullptr) return record_cuda(cudaErrorInvalidDevice);
   GemmArgs g;
@@ -517,7 +559,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   const int tiles = g.m_tiles * g.n_tiles;
   const int units = tiles < max_clusters[dev_id] ? tiles : max_clusters[dev_id];
   cfg.gridDim = dim3(static_cast<unsigned>(CG * units), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, ta, tb, td, g) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, ta, tb, td, tsa, tsb, g) != cudaSuccess)
     return record_cuda(cudaGetLastError());
   count_launch();
   return launch_status();
@@ -574,7 +616,7 @@ te_status te_gemm_mxfp8(const uint8_t* A, te_dtype fa, const uint8_t* sA, const 
   if (!sA || !sB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 32 + 3) / 4);
-  return launch_gemm<kMXFP8>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
+  return launch_gemm<kMXFP8, 1>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
                              f8_code(fb), static_cast<cudaStream_t>(stream));
 }
 
@@ -586,7 +628,7 @@ te_status te_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA, co
   if (!sA || !sB || !gA || !gB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 16 + 15) / 16) * 4;
-  return launch_gemm<kNVFP4>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
+  return launch_gemm<kNVFP4, 1>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
                              static_cast<cudaStream_t>(stream));
 }
 
