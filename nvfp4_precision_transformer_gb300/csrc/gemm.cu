@@ -9,29 +9,33 @@
 // Every kind moves 32 bytes of each operand row per instruction, so one k-tile
 // is a 128-byte row slice (one 128-byte-swizzle atom) and 4 instructions.
 //
-// CTA = 10 warps, one CTA per SM (the shared-memory footprint guarantees it):
+// CTA = 11 warps, one CTA per SM (the shared-memory footprint guarantees it):
 //   warp 0      TMA producer: A tile [128 x 128 B], B tile and, for the block-scaled
-//               kinds, the scale-factor atoms (bulk copies), into a shared-memory
-//               ring guarded by full/empty mbarriers;
-//   warp 1      allocates TMEM and issues the MMAs from one thread: scale factors
-//               are copied smem -> TMEM with tcgen05.cp, each k-tile's MMAs are
-//               followed by tcgen05.commit onto the stage's empty barrier, each
+//               kinds, the scale-factor atoms, into a shared-memory ring guarded by
+//               full/empty mbarriers;
+//   warp 1      allocates TMEM and issues the MMAs from one thread (for block-scaled
+//               kinds once the stage's scale factors are in TMEM): each k-tile's MMAs
+//               are followed by tcgen05.commit onto the stage's empty barrier, each
 //               tile's last k-tile by a commit onto the accumulator-full barrier;
 //   warps 2-9   epilogue: each warp owns a 32-lane quarter of TMEM and a 128-column
 //               half of the 128 x 256 accumulator, drains it to registers, releases
-//               the accumulator, then applies alpha / bias, rounds and stores.
-// BF16 and FP8 run as CTA pairs (2-CTA clusters, tcgen05 cta_group::2) on 256 x 256
-// tiles: each CTA stages 128 rows of A and 128 rows of B (6 stages), the leader's
-// thread issues M = 256 MMAs that read both CTAs' operands and write each CTA's 128
-// accumulator rows into its own TMEM, and its commits free the stage and publish the
-// accumulator in both CTAs; loads of both CTAs complete on the leader's full barrier,
-// and both CTAs' epilogue warps arrive on the leader's accumulator-empty barrier.
-// Halving each SM's share of B halves its shared-memory traffic for B.  MXFP8 and
-// NVFP4 run one CTA per 128 x 256 tile (4 / 3 stages of A [128 x 128 B] + B [256 x 128 B]):
-// their pair form (each CTA also stages the scale atoms of all 256 B rows, since each
-// half of a pair MMA reads every B row's scales from its own TMEM; scale atoms then
-// arrive by TMA so that they complete on the leader's barrier) is supported by the
-// template but measured 0-4 % slower, the per-SM scale-factor copies being unchanged.
+//               the accumulator, then applies alpha / bias, rounds and stores;
+//   warp 10     block-scaled kinds: issues the scale-factor copies (NVFP4 12, MXFP8 3 per
+//               k-tile) as soon as a stage lands and commits them onto the stage's
+//               sf_ready barrier, so the tensor pipe overlaps them with the MMAs of
+//               earlier k-tiles (copies and MMAs from one thread execute in issue order).
+// Every kind runs as CTA pairs (2-CTA clusters, tcgen05 cta_group::2) on 256 x 256
+// tiles: each CTA stages 128 rows of A and 128 rows of B (BF16 / FP8 / MXFP8 6 stages,
+// NVFP4 5), the leader's thread issues M = 256 MMAs that read both CTAs' operands and
+// write each CTA's 128 accumulator rows into its own TMEM, and its commits free the
+// stage and publish the accumulator in both CTAs; loads of both CTAs complete on the
+// leader's full barrier, and both CTAs' epilogue warps arrive on the leader's
+// accumulator-empty barrier.  Halving each SM's share of B halves its shared-memory
+// traffic for B.  Block-scaled kinds: each half of a pair MMA reads every B row's
+// scales from its own TMEM, so each CTA stages the scale atoms of all 256 B rows (and
+// its own 128 A rows); the pair tcgen05.cp copies each CTA's own shared memory into
+// its own TMEM; the atoms arrive by TMA so that they complete on the leader's barrier.
+// (The template also builds one CTA per 128 x 256 tile, CG = 1; no entry point uses it.)
 // The accumulator is double-buffered in TMEM for BF16/FP8 (2 x 256 columns); the
 // block-scaled kinds keep one 256-column accumulator plus a per-stage scale-factor
 // region and rely on the early release of the register drain for overlap.
@@ -49,7 +53,8 @@ enum Kind { kBF16 = 0, kFP8 = 1, kMXFP8 = 2, kNVFP4 = 3 };
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kCopyWarp = 2 + kEpiWarps;               // scale-factor copier (block-scaled kinds)
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int kGroupM = 8;
 
 // CG = 1: one CTA per 128 x 256 tile.  CG = 2 (BF16 / FP8): a CTA pair per 256 x 256
@@ -63,6 +68,9 @@ struct Cfg {
   static constexpr int kStages = kPair ? (KIND == kNVFP4 ? 5 : 6) : (KIND == kNVFP4 ? 3 : 4);
   static constexpr bool kBlockScaled = KIND >= kMXFP8;
   static constexpr int kAccStages = kBlockScaled ? 1 : 2;
+  // The scale copies (NVFP4 12, MXFP8 3 per k-tile) go out from a warp of their own,
+  // so the tensor pipe overlaps them with the MMAs (pairs: NVFP4 +12 %, MXFP8 +11 %).
+  static constexpr bool kSfCopier = kBlockScaled;
   static constexpr uint32_t kTmemCols = 512u;
   static constexpr int kABytes = BM * 128;
   static constexpr int kBBytes = kBRows * 128;
@@ -83,6 +91,7 @@ struct Cfg {
   static constexpr int kSmemStage = kSmemSfb + kStages * kSfbBytes;      // epilogue staging, 2 KB per warp
   static constexpr int kSmemBar = kSmemStage + kEpiWarps * 2048;
   static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
+  static_assert((3 * kStages + 5) * 8 + 8 <= 256, "barrier area");
   static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemTotal <= 232448, "shared memory budget");
 };
@@ -135,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_ready = drain + 1;  // [kStages]: the stage's scale factors are in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_ready + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -157,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::mbar_init(&acc_empty[s], kEpiWarps * CG);
     }
     dev::mbar_init(drain, 1);
+    for (int st = 0; st < kStages; ++st) dev::mbar_init(&sf_ready[st], 1);
     *abort_flag = 0;
     dev::fence_barrier_init();
     dev::prefetch_tmap(&tmA);
@@ -181,6 +192,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+
+  // Scale atoms of stage `st` (shared memory) -> its TMEM slot, one copy per 512-byte atom.
+  auto issue_sf_copies = [&](int st) {
+    const uint32_t sfa_t = tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
+    const uint32_t sfb_t = sfa_t + C::kSfaCols;
+    const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
+    const uint32_t sfb_s = dev::smem_u32(sSfb + st * C::kSfbBytes);
+    auto cp = [&](uint32_t t, uint32_t sa) {
+      if (kPair) dev::tc_cp_32x128b_x4_pair(t, dev::smem_desc(sa, 0, 128, 0));
+      else dev::tc_cp_32x128b_x4(t, dev::smem_desc(sa, 0, 128, 0));
+    };
+#pragma unroll
+    for (int j = 0; j < C::kSfAtoms; ++j) {
+      cp(sfa_t + 4 * j, sfa_s + 512 * j);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) cp(sfb_t + 8 * j + 4 * h, sfb_s + h * C::kSfAtoms * 512 + 512 * j);
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -280,21 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
-      auto copy_sf = [&](int st) {
-        const uint32_t sfa_t = sf_slot(st), sfb_t = sfa_t + C::kSfaCols;
-        const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
-        const uint32_t sfb_s = dev::smem_u32(sSfb + st * C::kSfbBytes);
-        auto cp = [&](uint32_t t, uint32_t sa) {
-          if (kPair) dev::tc_cp_32x128b_x4_pair(t, dev::smem_desc(sa, 0, 128, 0));
-          else dev::tc_cp_32x128b_x4(t, dev::smem_desc(sa, 0, 128, 0));
-        };
-#pragma unroll
-        for (int j = 0; j < C::kSfAtoms; ++j) {
-          cp(sfa_t + 4 * j, sfa_s + 512 * j);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) cp(sfb_t + 8 * j + 4 * h, sfb_s + h * C::kSfAtoms * 512 + 512 * j);
-        }
-      };
+      auto copy_sf = [&](int st) { issue_sf_copies(st); };
       for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
@@ -309,10 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // Scale factors of this k-tile into the stage's TMEM slot: from this thread (in
+          // issue order with the MMAs), or by the copier warp, whose copies run beside
+          // this thread's MMAs of the previous k-tiles.
+          if (C::kSfCopier && !dev::mbar_wait<kPair>(&sf_ready[stage], phase, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
           dev::tc_fence_after();
-          // Scale factors of this k-tile: smem -> TMEM slot of the stage.  tcgen05.cp and
-          // tcgen05.mma from this thread execute in issue order.
-          if (C::kBlockScaled) copy_sf(stage);
+          if (C::kBlockScaled && !C::kSfCopier) copy_sf(stage);
           const int nstage = stage + 1 == kStages ? 0 : stage + 1;
           const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
           const uint32_t a_addr = dev::smem_u32(sA + stage * C::kABytes);
@@ -356,6 +376,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit(drain, 1);
       volatile int dummy = 0;
       dev::mbar_wait(drain, 0, &dummy, args.err);
+    }
+  } else if (warp == kCopyWarp) {
+    // ------------------------------------------------ scale-factor copier (one thread; the pair's leader)
+    if (C::kSfCopier && lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = !*abort_flag;
+      int last = -1;
+      uint32_t last_phase = 0;
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+        for (int kt = 0; kt < args.k_tiles; ++kt) {
+          // full[stage] of this phase also means the MMAs that read the slot's previous
+          // contents have completed (the producer refilled the stage only after they did)
+          if (!dev::mbar_wait<kPair>(&full[stage], phase, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          dev::tc_fence_after();
+          issue_sf_copies(stage);
+          if (kPair) dev::tc_commit_pair(&sf_ready[stage], 1);
+          else dev::tc_commit(&sf_ready[stage]);
+          last = stage;
+          last_phase = phase;
+          if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+      }
+      if (!ok && last >= 0) {
+        // bounded wait for this thread's last copies before TMEM can be released
+        volatile int dummy = 0;
+        dev::mbar_wait<kPair>(&sf_ready[last], last_phase, &dummy, args.err);
+      }
     }
   } else {
     // ------------------------------------------------ epilogue warps
@@ -616,7 +667,7 @@ te_status te_gemm_mxfp8(const uint8_t* A, te_dtype fa, const uint8_t* sA, const 
   if (!sA || !sB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 32 + 3) / 4);
-  return launch_gemm<kMXFP8, 1>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
+  return launch_gemm<kMXFP8, 2>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
                              f8_code(fb), static_cast<cudaStream_t>(stream));
 }
 
@@ -628,7 +679,7 @@ te_status te_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA, co
   if (!sA || !sB || !gA || !gB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 16 + 15) / 16) * 4;
-  return launch_gemm<kNVFP4, 1>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
+  return launch_gemm<kNVFP4, 2>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
                              static_cast<cudaStream_t>(stream));
 }
 

@@ -214,17 +214,22 @@ class Layer:
         L.te_scale_update(self.recipe, 1, self.bwd.hist, self.bwd.amax, self.bwd.scale, self.bwd.scale_inv,
                           self.step_idx)
 
+    def run_linear(self, i: int, recipe: str, autocast: bool = True, on_gemm=None) -> None:
+        """The three GEMMs of linear ``i``; ``on_gemm(lin, pass_, phase)`` brackets each GEMM launch."""
+        lin = self.linears[i]
+        lin.sr_offset = self.step_idx
+        for p in PASSES:
+            if autocast:
+                lin.quantize(recipe, p)
+            if on_gemm:
+                on_gemm(lin, p, 0)
+            lin.gemm(recipe, p)
+            if on_gemm:
+                on_gemm(lin, p, 1)
+
     def run(self, recipe: str, autocast: bool = True, on_gemm=None) -> None:
-        """One layer's 12 GEMMs; ``on_gemm(lin, pass_, phase)`` brackets each GEMM launch."""
-        for lin in self.linears:
-            lin.sr_offset = self.step_idx
-            for p in PASSES:
-                if autocast:
-                    lin.quantize(recipe, p)
-                if on_gemm:
-                    on_gemm(lin, p, 0)
-                lin.gemm(recipe, p)
-                if on_gemm:
-                    on_gemm(lin, p, 1)
+        """One layer's 12 GEMMs, linear by linear, then the DelayedScaling update."""
+        for i in range(len(self.linears)):
+            self.run_linear(i, recipe, autocast, on_gemm)
         if autocast and recipe == "fp8_delayed":
             self.scale_update()
