@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace te {
@@ -262,41 +264,42 @@ __global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__
 // 8-byte patches with the next patch's loads in flight while it rotates the current
 // one; columns are rotated in pairs as packed fp32 values, and the 1/4 of the
 // transform is applied to the maximum (exact: scaling by 1/4 and rounding are monotone).
-template <typename T>
+template <typename T, int VB>
 __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                                float* amax, float* amax_rht, uint32_t signs) {
-  constexpr int PC = 8 / sizeof(T);  // columns per patch
+  using Vec = typename std::conditional<VB == 16, uint4, uint2>::type;
+  constexpr int PC = VB / sizeof(T);   // columns per patch
   const int64_t ncg = C / PC;
   const int64_t total = (R / 16) * ncg;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  auto load = [&](int64_t i, uint2 (&raw)[16]) {
+  auto load = [&](int64_t i, Vec (&raw)[16]) {
     if (i < total) {
       const int64_t band = i / ncg;
       const T* q = x + band * 16 * C + (i - band * ncg) * PC;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) raw[r] = __ldg(reinterpret_cast<const uint2*>(q + r * C));
+      for (int r = 0; r < 16; ++r) raw[r] = __ldg(reinterpret_cast<const Vec*>(q + r * C));
     }
   };
-  uint2 cur[16], nxt[16];
+  Vec cur[16], nxt[16];
   load(idx, cur);
   float m = 0.0f, mr = 0.0f;
   for (; idx < total; idx += stride) {
     load(idx + stride, nxt);
 #pragma unroll
-    for (int k = 0; k < (sizeof(T) == 2 ? 2 : 1); ++k) {  // column pairs of the patch
+    for (int k = 0; k < PC / 2; ++k) {  // column pairs of the patch
       float2 y[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         float lo, hi;
         if constexpr (sizeof(T) == 2) {
-          const uint32_t w = (k == 0 ? cur[r].x : cur[r].y) ^ rht_sign2(signs, r);
+          const uint32_t w = raw_word(cur[r], k) ^ rht_sign2(signs, r);
           lo = __uint_as_float(w << 16);
           hi = __uint_as_float(w & 0xFFFF0000u);
         } else {
           const uint32_t sg = (0u - ((signs >> r) & 1u)) & 0x80000000u;
-          lo = __uint_as_float(cur[r].x ^ sg);
-          hi = __uint_as_float(cur[r].y ^ sg);
+          lo = __uint_as_float(raw_word(cur[r], 2 * k) ^ sg);
+          hi = __uint_as_float(raw_word(cur[r], 2 * k + 1) ^ sg);
         }
         m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
         y[r] = make_float2(lo, hi);
@@ -311,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
   block_max_to(m, amax);
   block_max_to(__fmul_rn(mr, 0.25f), amax_rht);
 }
+
+// Vector width (bytes per patch row) of the rotated-amax kernel.
+constexpr int kRhtAmaxVB = 16;
 
 // ---- DelayedScaling update ----------------------------------------------------------------------
 __global__ void scale_update_kernel(int n, int L, int algo, int interval, float fmax, float margin_mul,
@@ -661,10 +667,10 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
           qb;
     }
   } else {
-  #pragma unroll 1
+#pragma unroll 1
     for (int b = 0; b < 64 / RB; ++b) {
       float v[NCL][RB];
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < RB; ++r) {
         const uint32_t w = tile_word(tile, b * RB + r, lane);
         if constexpr (sizeof(T) == 2) {
@@ -676,23 +682,23 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
       }
       float tile_m = 0.0f;
       if (two_d) {
-  #pragma unroll
+#pragma unroll
         for (int qq = 0; qq < NCL; ++qq)
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < RB; ++r) tile_m = fmaxf(tile_m, fabsf(v[qq][r]));
         tile_m = lanes_max<16 / NCL>(tile_m);  // 16 rows x 16 columns
       }
-  #pragma unroll
+#pragma unroll
       for (int q = 0; q < NCL; ++q) {
         const int cl = lane * NCL + q;  // column within the tile = row of the col-copy box
         if constexpr (FMT == kQE4M3 || FMT == kQE5M2) {
           if (track_max)
-  #pragma unroll
+#pragma unroll
             for (int r = 0; r < RB; ++r) lmax = fmaxf(lmax, fabsf(v[q][r]));
           *stage_chunk<G::COL_W>(box, cl, b) = fp8_pack16<FMT>(v[q], s_fp8);
         } else if constexpr (FMT == kQMX) {
           float m = 0.0f;
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < RB; ++r) m = fmaxf(m, fabsf(v[q][r]));
           const int E = mx_exponent(m);
           const float mult = mx_mult(E);
@@ -701,13 +707,13 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
           codes[q] |= static_cast<uint32_t>(E + 127) << (8 * b);
         } else {
           float x[16];
-  #pragma unroll
+#pragma unroll
           for (int r = 0; r < 16; ++r) x[r] = v[q][r];
           if (rht) rht16(x, a.signs);
           float m = tile_m;
           if (!two_d) {
             m = 0.0f;
-  #pragma unroll
+#pragma unroll
             for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(x[r]));
           }
           const uint32_t sc = nv_scale_code(m, senc);
@@ -862,14 +868,14 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
     return record_cuda(cudaGetLastError());
   if (rows * cols == 0) return TE_OK;
   if (amax_rht != nullptr) {
-    const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? 4 : 2));
+    const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? kRhtAmaxVB / 2 : kRhtAmaxVB / 4));
     const int64_t want = (patches + kThreads - 1) / kThreads;
     const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
     if (in == TE_BF16)
-      amax_rht_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, amax,
+      amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, amax,
                                                                 amax_rht, signs);
     else
-      amax_rht_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols, amax, amax_rht,
+      amax_rht_kernel<float, kRhtAmaxVB><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols, amax, amax_rht,
                                                         signs);
   } else if (in == TE_BF16) {
     amax_kernel<__nv_bfloat16, false><<<patch_blocks(rows, cols, 16, 8), kThreads, 0, st>>>(
