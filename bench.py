@@ -382,54 +382,30 @@ def main():
 
 def run_e2e(layer, args, ws):
     """The headline recipe end to end: every step copies the layer's inputs from pinned host
-    memory, runs it, and copies its outputs back.  Linear i's input copies (one stream) and
-    output copies (another) overlap the compute of its neighbours; events keep each linear's
-    device buffers from being overwritten before the previous step has read them."""
+    memory, runs it, and copies its outputs back (``HostStreamedLayer``: each linear's input
+    and output copies overlap its neighbours' compute)."""
     import torch
+    from nvfp4_precision_transformer_gb300.linear import HostStreamedLayer
     lins = layer.linears
-    n = len(lins)
     host_in = [(l.x.cpu().pin_memory(), l.w.cpu().pin_memory(), l.dy.cpu().pin_memory(),
                 l.bias.cpu().pin_memory()) for l in lins]
     host_out = [(torch.empty_like(l.y, device="cpu").pin_memory(), torch.empty_like(l.dx, device="cpu").pin_memory(),
                  torch.empty_like(l.dw, device="cpu").pin_memory()) for l in lins]
     h2d = sum(t.numel() * t.element_size() for tup in host_in for t in tup)
     d2h = sum(t.numel() * t.element_size() for tup in host_out for t in tup)
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k: [torch.cuda.Event() for _ in range(n)] for k in ("in", "comp", "out")}
-
-    def step():
-        for i, (l, (x, w, dy, b), (y, dx, dw)) in enumerate(zip(lins, host_in, host_out)):
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(ev["comp"][i])        # the previous step is done with these inputs
-                l.x.copy_(x, non_blocking=True)
-                l.w.copy_(w, non_blocking=True)
-                l.dy.copy_(dy, non_blocking=True)
-                l.bias.copy_(b, non_blocking=True)
-                ev["in"][i].record(s_in)
-            with torch.cuda.stream(s_comp):
-                s_comp.wait_event(ev["in"][i])
-                s_comp.wait_event(ev["out"][i])       # the previous step's outputs have left
-                layer.run_linear(i, HEADLINE[0], autocast=True)
-                ev["comp"][i].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev["comp"][i])
-                y.copy_(l.y, non_blocking=True)
-                dx.copy_(l.dx, non_blocking=True)
-                dw.copy_(l.dw, non_blocking=True)
-                ev["out"][i].record(s_out)
-
+    hs = HostStreamedLayer(layer, host_in, host_out)
     for _ in range(2):
-        step()
+        hs.step(HEADLINE[0])
     torch.cuda.synchronize()
     barrier(ws)
     main_s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main_s)
-    for s in (s_in, s_comp, s_out):
+    for s in hs.streams():
         s.wait_event(e0)
     for _ in range(args.e2e_steps):
-        step()
-    for s in (s_in, s_comp, s_out):
+        hs.step(HEADLINE[0])
+    for s in hs.streams():
         main_s.wait_stream(s)
     e1.record(main_s)
     torch.cuda.synchronize()

@@ -233,3 +233,53 @@ class Layer:
             self.run_linear(i, recipe, autocast, on_gemm)
         if autocast and recipe == "fp8_delayed":
             self.scale_update()
+
+
+class HostStreamedLayer:
+    """Runs a ``Layer`` whose inputs and outputs live in pinned host memory.
+
+    Per linear, the host-to-device copies of X, W, dY and the bias go on one stream,
+    the linear's three GEMMs (with their quantizers) on a second, and the device-to-host
+    copies of Y, dX and dW on a third.  Events order each linear's buffers across steps
+    (a step's input copies wait until the previous step's GEMMs of that linear are done;
+    its GEMMs wait until the previous step's outputs have left), so the transfers of one
+    linear overlap the compute of its neighbours.  ``host_in[i] = (x, w, dy, bias)`` and
+    ``host_out[i] = (y, dx, dw)`` are pinned CPU tensors shaped like the linear's buffers.
+    """
+
+    def __init__(self, layer: Layer, host_in, host_out):
+        import torch
+        self.layer, self.host_in, self.host_out = layer, host_in, host_out
+        self.s_in, self.s_comp, self.s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        n = len(layer.linears)
+        self.ev = {k: [torch.cuda.Event() for _ in range(n)] for k in ("in", "comp", "out")}
+
+    def streams(self):
+        return self.s_in, self.s_comp, self.s_out
+
+    def step(self, recipe: str, autocast: bool = True) -> None:
+        import torch
+        ev = self.ev
+        for i, (lin, (x, w, dy, b), (y, dx, dw)) in enumerate(zip(self.layer.linears, self.host_in, self.host_out)):
+            with torch.cuda.stream(self.s_in):
+                self.s_in.wait_event(ev["comp"][i])
+                lin.x.copy_(x, non_blocking=True)
+                lin.w.copy_(w, non_blocking=True)
+                lin.dy.copy_(dy, non_blocking=True)
+                if lin.bias is not None and b is not None:
+                    lin.bias.copy_(b, non_blocking=True)
+                ev["in"][i].record(self.s_in)
+            with torch.cuda.stream(self.s_comp):
+                self.s_comp.wait_event(ev["in"][i])
+                self.s_comp.wait_event(ev["out"][i])
+                self.layer.run_linear(i, recipe, autocast)
+                ev["comp"][i].record(self.s_comp)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(ev["comp"][i])
+                y.copy_(lin.y, non_blocking=True)
+                dx.copy_(lin.dx, non_blocking=True)
+                dw.copy_(lin.dw, non_blocking=True)
+                ev["out"][i].record(self.s_out)
+        if autocast and recipe == "fp8_delayed":
+            with torch.cuda.stream(self.s_comp):
+                self.layer.scale_update()
