@@ -141,6 +141,22 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
                           const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col,
                           float* amax_out, float* scale_inv_out, void* stream);
 
+/* Bias gradient fused with the FP8 quantization of dY ("How to Optimize Transformer-Based
+ * Models for Low-Precision Training": te.Linear(bias=True) layers; "Introduction to FP8
+ * training using Transformer Engine", section "Transformer Engine の使い方"): the same as
+ * te_quantize_fp8, and in the same read of x, dbias[c] = sum over rows r of x[r, c]
+ * (device fp32 [cols]).  Each 64-row tile's column sums (rows in order, fp32) go to
+ * `workspace` (device fp32, at least te_dbias_workspace_bytes(rows, cols) bytes, caller
+ * owned, 16-byte aligned, no initial contents needed: every entry is written); a second
+ * launch adds them over the tiles in order, so the result does not depend on timing.
+ * dbias NULL: exactly te_quantize_fp8.  rows == 0: dbias = 0.  Errors as te_quantize_fp8,
+ * plus TE_ERR_NULL (no workspace), TE_ERR_SHAPE (workspace too small), TE_ERR_ALIGN. */
+size_t te_dbias_workspace_bytes(int64_t rows, int64_t cols);
+te_status te_quantize_fp8_dbias(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                                const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col,
+                                float* amax_out, float* scale_inv_out, float* dbias, float* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* ---- MXFP8 ----------------------------------------------------------------------
  * Blocks of 32 consecutive elements along the contraction dimension (OCP MX
  * v1.0): E = clamp(floor(log2 a_b) - 8, -127, 127) (a_b = block amax; a_b = 0
@@ -194,6 +210,11 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
  * Common: A [M, K], B [N, K] contraction-major; D [M, N] row-major of out_dtype
  * (TE_BF16, round-to-nearest-even, or TE_F32); bias (nullable) device fp32 [N];
  * fp32 accumulation in tensor memory; epilogue D = alpha * acc + bias.
+ * accumulate = 1 (out_dtype TE_F32 only, else TE_ERR_DTYPE): D += alpha * acc + bias,
+ * the Wgrad form that adds into an fp32 main gradient (the pages' fp8_wgrad /
+ * weight-gradient path of "Introduction to FP8 training using Transformer Engine",
+ * NeMo keys); every element of D is read, added to in fp32 and written exactly once
+ * per call (a TMA reduce-add of the tile), so the result does not depend on timing.
  * M, N, K multiples of 16 (K of 32 for NVFP4).  Timing of the GEMM alone is the
  * pages' "pre-quantized" mode; quantize + GEMM is "autocast" mode. */
 
@@ -207,25 +228,25 @@ typedef enum {
  * Dgrad (dX = dY W: B = W read MN-major) and Wgrad (dW = dY^T X: both operands
  * MN-major) need no transposed copies, as a BF16 layer has none. */
 te_status te_gemm_bf16(const void* A, te_layout a_layout, const void* B, te_layout b_layout, const float* bias,
-                       void* D, te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
+                       void* D, te_dtype out_dtype, int accumulate, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* Per-tensor scaled FP8 (kind::f8f6f4): fa, fb in {TE_E4M3, TE_E5M2};
  * alpha = a_scale_inv[0] * b_scale_inv[0] (device fp32 scalars). */
 te_status te_gemm_fp8(const uint8_t* A, te_dtype fa, const uint8_t* B, te_dtype fb,
                       const float* a_scale_inv, const float* b_scale_inv, const float* bias, void* D,
-                      te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
+                      te_dtype out_dtype, int accumulate, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* MXFP8 (kind::mxf8f6f4, block 32, E8M0 scales in the tensor-core layout), alpha = 1.
  * sA: scales of A [M, K/32]; sB: scales of B [N, K/32]; K % 32 == 0. */
 te_status te_gemm_mxfp8(const uint8_t* A, te_dtype fa, const uint8_t* sA, const uint8_t* B, te_dtype fb,
-                        const uint8_t* sB, const float* bias, void* D, te_dtype out_dtype, int64_t M,
-                        int64_t N, int64_t K, void* stream);
+                        const uint8_t* sB, const float* bias, void* D, te_dtype out_dtype, int accumulate,
+                        int64_t M, int64_t N, int64_t K, void* stream);
 
 /* NVFP4 (kind::mxf4nvf4, block 16, UE4M3 scales in the tensor-core layout);
  * A, B packed E2M1 [M, K/2], [N, K/2]; alpha = gA[0] * gB[0] (the copies' S_dec). */
 te_status te_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA, const uint8_t* B,
                         const uint8_t* sB, const float* gB, const float* bias, void* D,
-                        te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream);
+                        te_dtype out_dtype, int accumulate, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* ---- host helpers ------------------------------------------------------------------ */
 

@@ -42,12 +42,15 @@ SIGNATURES = {
     "te_scale_update": (_st, [ctypes.POINTER(te_recipe), _int, _int, _vp, _vp, _vp, _vp, _i64, _vp]),
     "te_quantize_fp8": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp]),
     "te_quantize_mxfp8": (_st, [_vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "te_dbias_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "te_quantize_fp8_dbias": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    ctypes.c_size_t, _vp]),
     "te_quantize_nvfp4": (_st, [_vp, _int, _i64, _i64, _u32, _u32, _u64, _u64, _vp, _vp,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "te_gemm_bf16": (_st, [_vp, _int, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
-    "te_gemm_fp8": (_st, [_vp, _int, _vp, _int, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
-    "te_gemm_mxfp8": (_st, [_vp, _int, _vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
-    "te_gemm_nvfp4": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
+    "te_gemm_bf16": (_st, [_vp, _int, _vp, _int, _vp, _vp, _int, _int, _i64, _i64, _i64, _vp]),
+    "te_gemm_fp8": (_st, [_vp, _int, _vp, _int, _vp, _vp, _vp, _vp, _int, _int, _i64, _i64, _i64, _vp]),
+    "te_gemm_mxfp8": (_st, [_vp, _int, _vp, _vp, _int, _vp, _vp, _vp, _int, _int, _i64, _i64, _i64, _vp]),
+    "te_gemm_nvfp4": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _i64, _i64, _i64, _vp]),
     "te_scale_bytes": (ctypes.c_size_t, [_int, _i64, _i64]),
     "te_scale_unswizzle": (_st, [_int, _i64, _i64, _vp, _vp]),
     "te_status_str": (ctypes.c_char_p, [_int]),
@@ -143,6 +146,19 @@ def te_quantize_fp8(x, fmt: int, scale=None, compute_scale: int = 0, q_row=None,
                                                     _stream(stream)))
 
 
+def te_dbias_workspace_bytes(rows: int, cols: int) -> int:
+    return int(lib().te_dbias_workspace_bytes(rows, cols))
+
+
+def te_quantize_fp8_dbias(x, fmt: int, dbias, workspace, scale=None, compute_scale: int = 0, q_row=None, q_col=None,
+                          amax_out=None, scale_inv_out=None, stream=None):
+    r, c = _rc(x)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("te_quantize_fp8_dbias", lib().te_quantize_fp8_dbias(
+        _ptr(x), _in_dtype(x), r, c, fmt, _ptr(scale), compute_scale, _ptr(q_row), _ptr(q_col), _ptr(amax_out),
+        _ptr(scale_inv_out), _ptr(dbias), _ptr(workspace), nbytes, _stream(stream)))
+
+
 def te_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):
     r, c = _rc(x)
     _check("te_quantize_mxfp8", lib().te_quantize_mxfp8(_ptr(x), _in_dtype(x), r, c, _ptr(q_row), _ptr(s_row),
@@ -168,33 +184,38 @@ def _out_dtype(d):
     raise TypeError(f"unsupported output dtype {d.dtype}")
 
 
-def te_gemm_bf16(A, B, D, bias=None, a_layout: int = 0, b_layout: int = 0, stream=None):
+# accumulate=1: D (fp32) += the GEMM's result instead of D = result (Wgrad into a main
+# gradient); the library rejects it for a bf16 D.
+
+def te_gemm_bf16(A, B, D, bias=None, a_layout: int = 0, b_layout: int = 0, accumulate: int = 0, stream=None):
     """A is [M, K] (K_MAJOR) or [K, M] (MN_MAJOR); B is [N, K] or [K, N]; D is [M, N]."""
     M, N = D.shape
     K = A.shape[1] if a_layout == K_MAJOR else A.shape[0]
     _check("te_gemm_bf16", lib().te_gemm_bf16(_ptr(A), a_layout, _ptr(B), b_layout, _ptr(bias), _ptr(D),
-                                              _out_dtype(D), M, N, K, _stream(stream)))
+                                              _out_dtype(D), int(accumulate), M, N, K, _stream(stream)))
 
 
-def te_gemm_fp8(A, fa: int, B, fb: int, a_scale_inv, b_scale_inv, D, bias=None, stream=None):
+def te_gemm_fp8(A, fa: int, B, fb: int, a_scale_inv, b_scale_inv, D, bias=None, accumulate: int = 0, stream=None):
     M, K = A.shape
     N = B.shape[0]
     _check("te_gemm_fp8", lib().te_gemm_fp8(_ptr(A), fa, _ptr(B), fb, _ptr(a_scale_inv), _ptr(b_scale_inv),
-                                            _ptr(bias), _ptr(D), _out_dtype(D), M, N, K, _stream(stream)))
+                                            _ptr(bias), _ptr(D), _out_dtype(D), int(accumulate), M, N, K,
+                                            _stream(stream)))
 
 
-def te_gemm_mxfp8(A, sA, B, sB, D, bias=None, fa: int = E4M3, fb: int = E4M3, stream=None):
+def te_gemm_mxfp8(A, sA, B, sB, D, bias=None, fa: int = E4M3, fb: int = E4M3, accumulate: int = 0, stream=None):
     M, K = A.shape
     N = B.shape[0]
     _check("te_gemm_mxfp8", lib().te_gemm_mxfp8(_ptr(A), fa, _ptr(sA), _ptr(B), fb, _ptr(sB), _ptr(bias), _ptr(D),
-                                                _out_dtype(D), M, N, K, _stream(stream)))
+                                                _out_dtype(D), int(accumulate), M, N, K, _stream(stream)))
 
 
-def te_gemm_nvfp4(A, sA, gA, B, sB, gB, D, bias=None, stream=None):
+def te_gemm_nvfp4(A, sA, gA, B, sB, gB, D, bias=None, accumulate: int = 0, stream=None):
     M, Kh = A.shape
     N = B.shape[0]
     _check("te_gemm_nvfp4", lib().te_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(gA), _ptr(B), _ptr(sB), _ptr(gB),
-                                                _ptr(bias), _ptr(D), _out_dtype(D), M, N, 2 * Kh, _stream(stream)))
+                                                _ptr(bias), _ptr(D), _out_dtype(D), int(accumulate), M, N, 2 * Kh,
+                                                _stream(stream)))
 
 
 def te_scale_bytes(scale_fmt: int, rows: int, cols: int) -> int:

@@ -37,6 +37,10 @@ te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, u
 // shared-memory boxes, used for the GEMM epilogue's TMA stores).
 te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                              uint32_t box_inner_bytes, uint32_t box_rows);
+// fp32 matrix [rows, cols] with an unswizzled [box_rows, box_cols] box (element type
+// FLOAT32, as the TMA reduce-add needs).
+te_status make_tmap_2d_f32(CUtensorMap* map, const float* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                           uint32_t box_rows);
 // Same with the shared-memory box swizzled at its own width (64 B -> 64-byte
 // swizzle, 32 B -> 32-byte swizzle, 16 B -> none).
 te_status make_tmap_2d_boxswz(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
@@ -178,6 +182,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // TMA store of a shared-memory box to global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+// TMA reduce of a shared-memory box into global: D[y.., x..] += box (fp32 add, one
+// read-modify-write per element; bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");

@@ -108,6 +108,7 @@ struct GemmArgs {
   const float* bias;
   void* D;
   int out_f32;
+  int accumulate;       // 1: D (fp32) += result, by TMA reduce-add
   uint32_t idesc;
   int a_mn, b_mn;       // BF16 only: operand stored [K, M] / [K, N]
   int* err;
@@ -458,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          dev::tma_store_2d(&tmD, stg, nb * (args.out_f32 ? 4 : 2), m0);
+          if (args.accumulate) dev::tma_reduce_add_2d(&tmD, stg, nb, m0);
+          else dev::tma_store_2d(&tmD, stg, nb * (args.out_f32 ? 4 : 2), m0);
           dev::bulk_commit();
         }
       };
@@ -528,8 +530,8 @@ uint32_t make_idesc(int kind, uint32_t afmt, uint32_t bfmt, int m) {
 template <int KIND, int CG = 1>
 te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uint8_t* sfa, const uint8_t* sfb,
                       int64_t sf_katoms, const float* alpha_a, const float* alpha_b, const float* bias, void* D,
-                      te_dtype out, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, cudaStream_t st,
-                      int a_mn = 0, int b_mn = 0) {
+                      te_dtype out, int accumulate, int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt,
+                      cudaStream_t st, int a_mn = 0, int b_mn = 0) {
   using C = Cfg<KIND, CG>;
   static bool attr_set[64] = {false};
   static int max_clusters[64] = {0};
@@ -572,7 +574,10 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   if (s != TE_OK) return s;
   CUtensorMap td;
   const uint32_t esize = out == TE_F32 ? 4u : 2u;
-  s = make_tmap_2d_plain(&td, D, static_cast<uint64_t>(N) * esize, static_cast<uint64_t>(M), 64u, 32u);
+  // accumulate: an fp32-typed map (the reduce-add needs the element type), box 16 x 32
+  s = accumulate ? make_tmap_2d_f32(&td, static_cast<const float*>(D), static_cast<uint64_t>(N),
+                                    static_cast<uint64_t>(M), 16u, 32u)
+                 : make_tmap_2d_plain(&td, D, static_cast<uint64_t>(N) * esize, static_cast<uint64_t>(M), 64u, 32u);
   if (s != TE_OK) return s;
   // scale tensors as 256-byte rows (CTA pairs load them by TMA); unused otherwise
   CUtensorMap tsa = td, tsb = td;
@@ -603,6 +608,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.bias = bias;
   g.D = D;
   g.out_f32 = out == TE_F32;
+  g.accumulate = accumulate;
   g.idesc = make_idesc(KIND, afmt, bfmt, BM * CG) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
   g.a_mn = a_mn;
   g.b_mn = b_mn;
@@ -616,9 +622,11 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   return launch_status();
 }
 
-te_status check_gemm(const void* A, const void* B, const void* D, te_dtype out, int64_t M, int64_t N, int64_t K,
-                     int64_t k_multiple) {
+te_status check_gemm(const void* A, const void* B, const void* D, te_dtype out, int accumulate, int64_t M, int64_t N,
+                     int64_t K, int64_t k_multiple) {
   if (out != TE_BF16 && out != TE_F32) return TE_ERR_DTYPE;
+  if (accumulate != 0 && accumulate != 1) return TE_ERR_ARG;
+  if (accumulate && out != TE_F32) return TE_ERR_DTYPE;
   if (M < 0 || N < 0 || K <= 0 || M % 16 || N % 16 || K % k_multiple) return TE_ERR_SHAPE;
   if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return TE_ERR_SHAPE;
   if (M * N == 0) return TE_OK;
@@ -638,49 +646,50 @@ using namespace te;
 extern "C" {
 
 te_status te_gemm_bf16(const void* A, te_layout a_layout, const void* B, te_layout b_layout, const float* bias, void* D,
-                       te_dtype out_dtype, int64_t M, int64_t N, int64_t K, void* stream) {
+                       te_dtype out_dtype, int accumulate, int64_t M, int64_t N, int64_t K, void* stream) {
   if ((a_layout != TE_K_MAJOR && a_layout != TE_MN_MAJOR) || (b_layout != TE_K_MAJOR && b_layout != TE_MN_MAJOR))
     return TE_ERR_ARG;
-  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
+  te_status s = check_gemm(A, B, D, out_dtype, accumulate, M, N, K, 16);
   if (s != TE_OK || M * N == 0) return s;
-  return launch_gemm<kBF16, 2>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, M, N, K, 1u, 1u,
-                            static_cast<cudaStream_t>(stream), a_layout == TE_MN_MAJOR, b_layout == TE_MN_MAJOR);
+  return launch_gemm<kBF16, 2>(A, B, K * 2, nullptr, nullptr, 0, nullptr, nullptr, bias, D, out_dtype, accumulate, M, N,
+                               K, 1u, 1u, static_cast<cudaStream_t>(stream), a_layout == TE_MN_MAJOR,
+                               b_layout == TE_MN_MAJOR);
 }
 
 te_status te_gemm_fp8(const uint8_t* A, te_dtype fa, const uint8_t* B, te_dtype fb, const float* a_scale_inv,
-                      const float* b_scale_inv, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
-                      int64_t K, void* stream) {
+                      const float* b_scale_inv, const float* bias, void* D, te_dtype out_dtype, int accumulate,
+                      int64_t M, int64_t N, int64_t K, void* stream) {
   if (!fp8_fmt(fa) || !fp8_fmt(fb)) return TE_ERR_DTYPE;
-  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 16);
+  te_status s = check_gemm(A, B, D, out_dtype, accumulate, M, N, K, 16);
   if (s != TE_OK || M * N == 0) return s;
   if (!a_scale_inv || !b_scale_inv) return TE_ERR_NULL;
-  return launch_gemm<kFP8, 2>(A, B, K, nullptr, nullptr, 0, a_scale_inv, b_scale_inv, bias, D, out_dtype, M, N, K,
-                           f8_code(fa), f8_code(fb), static_cast<cudaStream_t>(stream));
+  return launch_gemm<kFP8, 2>(A, B, K, nullptr, nullptr, 0, a_scale_inv, b_scale_inv, bias, D, out_dtype, accumulate, M,
+                              N, K, f8_code(fa), f8_code(fb), static_cast<cudaStream_t>(stream));
 }
 
 te_status te_gemm_mxfp8(const uint8_t* A, te_dtype fa, const uint8_t* sA, const uint8_t* B, te_dtype fb,
-                        const uint8_t* sB, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
-                        int64_t K, void* stream) {
+                        const uint8_t* sB, const float* bias, void* D, te_dtype out_dtype, int accumulate,
+                        int64_t M, int64_t N, int64_t K, void* stream) {
   if (!fp8_fmt(fa) || !fp8_fmt(fb)) return TE_ERR_DTYPE;
-  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 32);
+  te_status s = check_gemm(A, B, D, out_dtype, accumulate, M, N, K, 32);
   if (s != TE_OK || M * N == 0) return s;
   if (!sA || !sB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 32 + 3) / 4);
-  return launch_gemm<kMXFP8, 2>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, M, N, K, f8_code(fa),
-                             f8_code(fb), static_cast<cudaStream_t>(stream));
+  return launch_gemm<kMXFP8, 2>(A, B, K, sA, sB, katoms, nullptr, nullptr, bias, D, out_dtype, accumulate, M, N, K,
+                                f8_code(fa), f8_code(fb), static_cast<cudaStream_t>(stream));
 }
 
 te_status te_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA, const uint8_t* B, const uint8_t* sB,
-                        const float* gB, const float* bias, void* D, te_dtype out_dtype, int64_t M, int64_t N,
-                        int64_t K, void* stream) {
-  te_status s = check_gemm(A, B, D, out_dtype, M, N, K, 32);
+                        const float* gB, const float* bias, void* D, te_dtype out_dtype, int accumulate,
+                        int64_t M, int64_t N, int64_t K, void* stream) {
+  te_status s = check_gemm(A, B, D, out_dtype, accumulate, M, N, K, 32);
   if (s != TE_OK || M * N == 0) return s;
   if (!sA || !sB || !gA || !gB) return TE_ERR_NULL;
   if (!aligned16(sA) || !aligned16(sB)) return TE_ERR_ALIGN;
   const int64_t katoms = ((K / 16 + 15) / 16) * 4;
-  return launch_gemm<kNVFP4, 2>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, M, N, K, 1u, 1u,
-                             static_cast<cudaStream_t>(stream));
+  return launch_gemm<kNVFP4, 2>(A, B, K / 2, sA, sB, katoms, gA, gB, bias, D, out_dtype, accumulate, M, N, K, 1u, 1u,
+                                static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -77,8 +77,9 @@ int num_sms() {
   return g_sms[d];
 }
 
-static te_status encode_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_inner,
-                           uint32_t box_rows, CUtensorMapSwizzle swz) {
+static te_status encode_2d_typed(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t elem_bytes,
+                                 uint64_t cols, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                                 CUtensorMapSwizzle swz) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_encode == nullptr) {
@@ -91,15 +92,20 @@ static te_status encode_2d(CUtensorMap* map, const void* base, uint64_t row_byte
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
   }
-  cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return record_cuda(cudaErrorInvalidValue);
   return TE_OK;
+}
+
+static te_status encode_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_inner,
+                           uint32_t box_rows, CUtensorMapSwizzle swz) {
+  return encode_2d_typed(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, row_bytes, rows, box_inner, box_rows, swz);
 }
 
 te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
@@ -109,6 +115,12 @@ te_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, u
 te_status make_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                              uint32_t box_inner_bytes, uint32_t box_rows) {
   return encode_2d(map, base, row_bytes, rows, box_inner_bytes, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+te_status make_tmap_2d_f32(CUtensorMap* map, const float* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                           uint32_t box_rows) {
+  return encode_2d_typed(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, box_cols, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 te_status make_tmap_2d_boxswz(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,

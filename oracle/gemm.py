@@ -31,6 +31,17 @@ def gemm(a_deq, b_deq, alpha: float = 1.0, bias=None) -> np.ndarray:
     return d
 
 
+def gemm_accumulate(d_old, a_deq, b_deq, alpha: float = 1.0, bias=None) -> np.ndarray:
+    """Wgrad accumulated into an fp32 main gradient: D_new = D_old + alpha * A @ B^T (+ bias).
+
+    The weight gradient of successive micro-batches is summed into one fp32 buffer
+    (the NeMo ``fp8_wgrad`` key of "Introduction to FP8 training using Transformer
+    Engine", section "Transformer Engine 統合済みライブラリの利用").  fp64 here; the
+    device adds once per element in fp32.
+    """
+    return np.asarray(d_old, dtype=np.float64) + gemm(a_deq, b_deq, alpha, bias)
+
+
 def linear_shapes(hidden: int, ffn: int, tokens: int):
     """The 12 GEMM shapes (name, pass, M, N, K) of one transformer layer's linears.
 

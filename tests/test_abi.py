@@ -60,14 +60,17 @@ def test_validation_before_any_device_work(lib):
     assert lib.te_quantize_nvfp4(fake, L.BF16, 32, 32, 8, 0, 0, 0, fake, fake, fake, fake, fake,
                                  None, None, None, None) == 8
     # GEMMs: shapes, K == 0, dtype
-    assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.BF16, 32, 40, 32, None) == 2
-    assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.BF16, 32, 32, 0, None) == 2
-    assert lib.te_gemm_bf16(fake, 2, fake, 0, None, fake, L.BF16, 32, 32, 32, None) == 8
-    assert lib.te_gemm_fp8(fake, L.E2M1, fake, L.E4M3, fake, fake, None, fake, L.BF16, 32, 32, 32, None) == 4
-    assert lib.te_gemm_nvfp4(fake, fake, fake, fake, fake, fake, None, fake, L.BF16, 32, 32, 48, None) == 2
-    assert lib.te_gemm_mxfp8(fake, L.E4M3, fake, fake, L.E4M3, fake, None, fake, L.E8M0, 32, 32, 32, None) == 4
+    assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.BF16, 0, 32, 40, 32, None) == 2
+    assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.BF16, 0, 32, 32, 0, None) == 2
+    assert lib.te_gemm_bf16(fake, 2, fake, 0, None, fake, L.BF16, 0, 32, 32, 32, None) == 8
+    assert lib.te_gemm_fp8(fake, L.E2M1, fake, L.E4M3, fake, fake, None, fake, L.BF16, 0, 32, 32, 32, None) == 4
+    assert lib.te_gemm_nvfp4(fake, fake, fake, fake, fake, fake, None, fake, L.BF16, 0, 32, 32, 48, None) == 2
+    assert lib.te_gemm_mxfp8(fake, L.E4M3, fake, fake, L.E4M3, fake, None, fake, L.E8M0, 0, 32, 32, 32, None) == 4
+    # accumulate adds into an fp32 D only; any flag other than 0 / 1 is rejected
+    assert lib.te_gemm_fp8(fake, L.E4M3, fake, L.E4M3, fake, fake, None, fake, L.BF16, 1, 32, 32, 32, None) == 4
+    assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.F32, 2, 32, 32, 32, None) == 8
     # empty GEMM is a no-op success
-    assert lib.te_gemm_bf16(None, 0, None, 0, None, None, L.BF16, 0, 32, 32, None) == 0
+    assert lib.te_gemm_bf16(None, 0, None, 0, None, None, L.BF16, 0, 0, 32, 32, None) == 0
     # recipe validation
     r = L.te_recipe(L.E4M3, L.E5M2, 0, 0, 0, 1)
     assert lib.te_scale_update(ctypes.byref(r), 0, 4, fake, fake, fake, fake, 0, None) == 8

@@ -318,3 +318,59 @@ def test_gemm_rejects_bad_shapes():
     with pytest.raises(te.TEError) as ei:
         te.te_gemm_bf16(A, torch.zeros(32, 40, dtype=torch.bfloat16, device=G.DEV), D)   # K = 40
     assert ei.value.status == 2
+
+
+# ---- Wgrad accumulated into an fp32 main gradient -----------------------------------------------
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "mxfp8", "nvfp4"])
+def test_wgrad_accumulates_into_fp32_main_grad(kind):
+    # two micro-batches of tokens; dW of each is added into one fp32 buffer that already
+    # holds a gradient, in place (accumulate=1): D = D0 + dW_1 + dW_2
+    M, Kin, Nout = 256, 288, 224
+    rng = np.random.default_rng(17)
+    d0 = (rng.standard_normal((Nout, Kin)) * 0.01).astype(np.float32)
+    D = torch.from_numpy(d0.copy()).to(G.DEV)
+    ref = d0.astype(np.float64)
+    for mb in range(2):
+        x, w, dy, b = _linear(M, Kin, Nout, 700 + 10 * mb)
+        x32, dy32 = G.f32_np(x), G.f32_np(dy)
+        if kind == "bf16":
+            te.te_gemm_bf16(dy, x, D, None, a_layout=te.MN_MAJOR, b_layout=te.MN_MAJOR, accumulate=1)
+            A64, B64 = dy32.T, x32.T
+        elif kind == "fp8":
+            _, dc, ds = _fp8_current(dy, "e5m2")
+            _, xc, xs = _fp8_current(x, "e4m3")
+            te.te_gemm_fp8(dc, te.E5M2, xc, te.E4M3, ds, xs, D, accumulate=1)
+            A64, B64 = _fp8_oracle(dy32, "e5m2")[1], _fp8_oracle(x32, "e4m3")[1]
+        elif kind == "mxfp8":
+            _, _, dc, dsc = _mx(dy)
+            _, _, xc, xsc = _mx(x)
+            te.te_gemm_mxfp8(dc, dsc, xc, xsc, D, accumulate=1)
+            A64, B64 = _mx_oracle(dy32)[1], _mx_oracle(x32)[1]
+        else:
+            dq = _nv(dy, te.NVFP4_RHT_COL)
+            xq = _nv(x, te.NVFP4_RHT_COL)
+            te.te_gemm_nvfp4(dq[3], dq[4], dq[5], xq[3], xq[4], xq[5], D, accumulate=1)
+            A64 = _nv_oracle(dy32, te.NVFP4_RHT_COL)[1]
+            B64 = _nv_oracle(x32, te.NVFP4_RHT_COL)[1]
+        torch.cuda.synchronize()
+        ref = OG.gemm_accumulate(ref, A64, B64)
+    got = D.cpu().numpy().astype(np.float64)
+    # the bar applies to the accumulated increment (the product); D0 itself must survive
+    err = OG.rel_frobenius(got - d0, ref - d0)
+    assert err <= TOL, f"{kind} wgrad accumulate: rel-Frobenius {err:.3e}"
+    G.check_no_device_error()
+
+
+def test_accumulate_of_zero_product_keeps_main_grad_bits():
+    M, N, K = 256, 256, 128
+    d0 = np.random.default_rng(2).standard_normal((M, N)).astype(np.float32)
+    D = torch.from_numpy(d0.copy()).to(G.DEV)
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device=G.DEV)
+    B = torch.zeros(N, K, dtype=torch.bfloat16, device=G.DEV)
+    te.te_gemm_bf16(A, B, D, None, accumulate=1)
+    te.te_gemm_bf16(A, B, D, None, accumulate=1)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(D.cpu().numpy().view(np.uint32), d0.view(np.uint32))
+    with pytest.raises(te.TEError):
+        te.te_gemm_bf16(A, B, torch.empty(M, N, dtype=torch.bfloat16, device=G.DEV), None, accumulate=1)

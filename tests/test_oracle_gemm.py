@@ -67,3 +67,20 @@ def test_rel_frobenius_and_bf16_rounding():
     bf = F.bf16_bits_to_f32(F.f64_to_bf16_bits(ref))
     e = G.rel_frobenius(bf, ref)
     assert 5e-4 < e < 3e-3                        # bf16 output rounding alone is ~1.7e-3
+
+
+def test_gemm_accumulate_sums_micro_batches():
+    # splitting the contraction (the token dimension of Wgrad) into micro-batches and
+    # accumulating gives the full product: sum_j A_j^T B_j over token blocks j
+    rng = np.random.default_rng(5)
+    dy = rng.standard_normal((96, 12))      # tokens x out
+    x = rng.standard_normal((96, 20))       # tokens x in
+    full = dy.T @ x                          # out x in
+    acc = np.zeros((12, 20))
+    for j in range(0, 96, 32):
+        acc = G.gemm_accumulate(acc, dy[j:j + 32].T, x[j:j + 32].T)
+    np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-12)
+    # zero operands leave D unchanged; identity operands add B
+    d0 = rng.standard_normal((4, 4))
+    assert np.array_equal(G.gemm_accumulate(d0, np.zeros((4, 3)), np.zeros((4, 3))), d0)
+    np.testing.assert_array_equal(G.gemm_accumulate(d0, np.eye(4), np.eye(4)), d0 + np.eye(4))
