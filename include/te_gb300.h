@@ -148,7 +148,7 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
  * (device fp32 [cols]).  Each 64-row tile's column sums (rows in order, fp32) go to
  * `workspace` (device fp32, at least te_dbias_workspace_bytes(rows, cols) bytes, caller
  * owned, 16-byte aligned, no initial contents needed: every entry is written); a second
- * launch adds them over the tiles in order, so the result does not depend on timing.
+ * launch adds them over the tiles in a fixed order, so the result does not depend on timing.
  * dbias NULL: exactly te_quantize_fp8.  rows == 0: dbias = 0.  Errors as te_quantize_fp8,
  * plus TE_ERR_NULL (no workspace), TE_ERR_SHAPE (workspace too small), TE_ERR_ALIGN. */
 size_t te_dbias_workspace_bytes(int64_t rows, int64_t cols);

@@ -179,25 +179,13 @@ struct Chunk<float, 16> {
   using Raw = uint4;
   static constexpr int N = 4;
 };
-template <>
-struct Chunk<__nv_bfloat16, 8> {
-  using Raw = uint2;
-  static constexpr int N = 4;
-};
-template <>
-struct Chunk<float, 8> {
-  using Raw = uint2;
-  static constexpr int N = 2;
-};
 
 __device__ __forceinline__ uint4 ld_raw(const uint4* p) { return __ldg(p); }
-__device__ __forceinline__ uint2 ld_raw(const uint2* p) { return __ldg(p); }
 __device__ __forceinline__ void zero_raw(uint4& r) { r = make_uint4(0, 0, 0, 0); }
-__device__ __forceinline__ void zero_raw(uint2& r) { r = make_uint2(0, 0); }
 __device__ __forceinline__ uint32_t raw_word(const uint4& r, int k) {
   return k == 0 ? r.x : (k == 1 ? r.y : (k == 2 ? r.z : r.w));
 }
-__device__ __forceinline__ uint32_t raw_word(const uint2& r, int k) { return k == 0 ? r.x : r.y; }
+[[maybe_unused]] __device__ __forceinline__ uint32_t raw_word(const uint2& r, int k) { return k == 0 ? r.x : r.y; }
 
 template <typename T, typename Raw>
 __device__ __forceinline__ float elem(const Raw& r, int i) {
@@ -342,6 +330,27 @@ __global__ void scale_update_kernel(int n, int L, int algo, int interval, float 
   scale_inv[i] = __fdiv_rn(1.0f, s);
 }
 
+// Bias gradient from the per-tile partial sums.  A CTA owns 32 columns; its 8 warps sum
+// the tile rows t = w, w + 8, w + 16, ... in order, then warp 0 adds the 8 partial
+// sums in warp order -- a fixed order, so the result does not depend on timing.
+__global__ void __launch_bounds__(256) dbias_reduce_kernel(const float* __restrict__ ws, int64_t tiles_r, int64_t C,
+                                                           float* __restrict__ dbias) {
+  __shared__ float part[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  float s = 0.0f;
+  if (c < C)
+    for (int64_t t = w; t < tiles_r; t += 8) s = __fadd_rn(s, __ldg(ws + t * C + c));
+  part[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < C) {
+    float r = part[0][lane];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) r = __fadd_rn(r, part[k][lane]);
+    dbias[c] = r;
+  }
+}
+
 __device__ __forceinline__ float current_scale(float a, float fmax) {
   if (!(isfinite(a) && a > 0.0f)) return 1.0f;
   const float s = __fdiv_rn(fmax, a);
@@ -402,6 +411,8 @@ struct TileArgs {
   const float* amax_rht;
   float* gdec_row;
   float* gdec_col;
+  // column sums (bias gradient): per 64-row tile, partial sums into ws[tile_row][C]
+  float* dbias_ws;
   int* err;
 };
 
@@ -511,6 +522,30 @@ struct QSmem {
   static_assert(kTotal <= 232448, "shared memory budget");
   static_assert(G::ROW_BOX % 1024 == 0 && G::COL_BOX % 1024 == 0, "box alignment");
 };
+
+// Column sums of one input tile (rows in order 0..63, fp32) for the bias gradient:
+// lane l sums its 4-byte column slice (two bf16 columns or one fp32 column) and
+// writes the tile row's partial sums; rows past the tensor's end were zero-filled.
+template <typename T>
+__device__ __forceinline__ void tile_colsum(const uint8_t* tile, int64_t r0, int64_t c0, const TileArgs& a, int lane) {
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 16
+  for (int r = 0; r < 64; ++r) {
+    const uint32_t w = tile_word(tile, r, lane);
+    if constexpr (sizeof(T) == 2) {
+      s0 = __fadd_rn(s0, __uint_as_float(w << 16));
+      s1 = __fadd_rn(s1, __uint_as_float(w & 0xFFFF0000u));
+    } else {
+      s0 = __fadd_rn(s0, __uint_as_float(w));
+    }
+  }
+  constexpr int NCL = 4 / sizeof(T);
+  const int64_t col = c0 + lane * NCL;
+  if (col >= a.C) return;
+  float* dst = a.dbias_ws + (r0 / 64) * a.C + col;
+  if constexpr (sizeof(T) == 2) *reinterpret_cast<float2*>(dst) = make_float2(s0, s1);
+  else *dst = s0;
+}
 
 // Row copy of one tile: lane handles rows lane and lane + 32.
 template <typename T, int FMT, bool SR>
@@ -813,6 +848,7 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
     __syncwarp();
     if (a.do_row) row_pass<T, FMT, SR>(tile, box_row, r0, c0, a, s_fp8, senc_r, rtab, lane, lmax);
     if (a.do_col) col_pass<T, FMT, SR>(tile, box_col, r0, c0, a, s_fp8, senc_c, rtab + 128, lane, lmax, !a.do_row);
+    if (a.dbias_ws != nullptr) tile_colsum<T>(tile, r0, c0, a, lane);
     dev::fence_proxy_async();  // order this tile's shared-memory reads and box writes before the async copies
     __syncwarp();
     if (lane == 0) {
@@ -989,21 +1025,37 @@ te_status te_scale_update(const te_recipe* recipe, int is_backward, int n_tensor
   return launch_status();
 }
 
-te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
-                          const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col, float* amax_out,
-                          float* scale_inv_out, void* stream) {
+size_t te_dbias_workspace_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return static_cast<size_t>((rows + 63) / 64) * static_cast<size_t>(cols) * sizeof(float);
+}
+
+te_status te_quantize_fp8_dbias(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                                const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col, float* amax_out,
+                                float* scale_inv_out, float* dbias, float* workspace, size_t workspace_bytes,
+                                void* stream) {
   te_status s = check_2d(x, in_dtype, rows, cols);
   if (s != TE_OK) return s;
   if (fmt != TE_E4M3 && fmt != TE_E5M2) return TE_ERR_DTYPE;
   if (compute_scale != 0 && compute_scale != 1) return TE_ERR_ARG;
   if (compute_scale ? amax_out == nullptr : scale == nullptr) return TE_ERR_NULL;
   if ((q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col))) return TE_ERR_ALIGN;
+  const bool want_dbias = dbias != nullptr;
+  if (want_dbias && cols > 0) {
+    if (rows > 0 && workspace == nullptr) return TE_ERR_NULL;
+    if (rows > 0 && workspace_bytes < te_dbias_workspace_bytes(rows, cols)) return TE_ERR_SHAPE;
+    if ((rows > 0 && !aligned16(workspace)) || (reinterpret_cast<uintptr_t>(dbias) & 3u)) return TE_ERR_ALIGN;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (compute_scale) {
     s = launch_amax(x, in_dtype, rows, cols, amax_out, nullptr, 0, st);
     if (s != TE_OK) return s;
   } else if (amax_out != nullptr) {
     if (cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess) return record_cuda(cudaGetLastError());
+  }
+  if (want_dbias && rows == 0 && cols > 0) {
+    if (cudaMemsetAsync(dbias, 0, static_cast<size_t>(cols) * sizeof(float), st) != cudaSuccess)
+      return record_cuda(cudaGetLastError());
   }
   if (rows * cols == 0 && scale_inv_out == nullptr) return TE_OK;
   // An empty tensor still launches one (load-free) CTA so that scale_inv_out is published.
@@ -1016,8 +1068,21 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
   a.fmax = fmt == TE_E4M3 ? 448.0f : 57344.0f;
   a.amax_out = compute_scale ? nullptr : amax_out;
   a.scale_inv_out = scale_inv_out;
-  if (fmt == TE_E4M3) return launch_qtile_any<kQE4M3, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
-  return launch_qtile_any<kQE5M2, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
+  a.dbias_ws = (want_dbias && rows * cols > 0) ? workspace : nullptr;
+  s = fmt == TE_E4M3 ? launch_qtile_any<kQE4M3, false>(x, in_dtype, rows, cols, q_row, q_col, a, st)
+                     : launch_qtile_any<kQE5M2, false>(x, in_dtype, rows, cols, q_row, q_col, a, st);
+  if (s != TE_OK || a.dbias_ws == nullptr) return s;
+  const int64_t tiles_r = (rows + 63) / 64;
+  dbias_reduce_kernel<<<static_cast<unsigned>((cols + 31) / 32), 256, 0, st>>>(workspace, tiles_r, cols, dbias);
+  count_launch();
+  return launch_status();
+}
+
+te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                          const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col, float* amax_out,
+                          float* scale_inv_out, void* stream) {
+  return te_quantize_fp8_dbias(x, in_dtype, rows, cols, fmt, scale, compute_scale, q_row, q_col, amax_out,
+                               scale_inv_out, nullptr, nullptr, 0, stream);
 }
 
 te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint8_t* q_row,

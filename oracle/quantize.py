@@ -46,6 +46,18 @@ def amax(x) -> np.float32:
     return f32(np.max(np.abs(x)))
 
 
+# ---- bias gradient -------------------------------------------------------------
+
+def dbias(dy) -> np.ndarray:
+    """Bias gradient of Y = X W^T + b: dbias[n] = sum over tokens m of dY[m, n] (fp64).
+
+    te.Linear(768, 768, bias=True) of "Introduction to FP8 training using Transformer
+    Engine", section "Transformer Engine の使い方": the bias receives the column sums of
+    the output gradient; fusing them into dY's quantization is the adjacent backward step.
+    """
+    return np.asarray(dy, dtype=np.float64).sum(axis=0)
+
+
 # ---- per-tensor FP8 ------------------------------------------------------------
 
 def fp8_cast(x, scale, fmt: str) -> np.ndarray:

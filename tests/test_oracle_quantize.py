@@ -278,3 +278,14 @@ def test_nvfp4_sr_uses_copy_indexed_words():
     np.testing.assert_array_equal(q_full[8:16], q_part)
     q_rn, _, _ = Q.nvfp4_quantize(z, A)
     assert np.mean(q_rn != q_full) > 0.05       # SR really differs from RN on random data
+
+
+def test_dbias_closed_forms_and_loops():
+    # ones -> number of rows; column j of value j * (row index) -> j * R (R - 1) / 2
+    R, C = 37, 5
+    np.testing.assert_array_equal(Q.dbias(np.ones((R, C), np.float32)), np.full(C, float(R)))
+    t = np.arange(R)[:, None] * np.arange(C)[None, :]
+    np.testing.assert_array_equal(Q.dbias(t), np.arange(C) * R * (R - 1) / 2)
+    x = rng.standard_normal((9, 4)).astype(np.float32)
+    brute = [sum(float(x[r, c]) for r in range(9)) for c in range(4)]
+    np.testing.assert_allclose(Q.dbias(x), brute, rtol=0, atol=1e-12)
