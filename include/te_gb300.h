@@ -206,6 +206,24 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
                             uint8_t* q_row, uint8_t* s_row, float* gdec_row,
                             uint8_t* q_col, uint8_t* s_col, float* gdec_col, void* stream);
 
+/* te_quantize_fp8_dbias without a caller workspace.  The paper has no counterpart: this
+ * exists for callers that cannot allocate device memory where they quantize dY -- code
+ * running while a memory pool is locked or sized ahead of time, or a host runtime that
+ * owns every allocation and passes only the tensors to be computed on.  The 64-row-tile
+ * partial sums go to a fixed 4 MiB array inside the library (one per GPU that loads the
+ * library, kept until the process exits), so ceil(rows / 64) * cols may be at most
+ * 1,048,576 (e.g. 15872 x 4096); larger requests return TE_ERR_SHAPE before anything is
+ * enqueued.  Arguments, outputs and other errors as te_quantize_fp8_dbias.  Nothing in
+ * the array has to start at zero (each call writes every partial sum it reads), but
+ * every call shares it: calls that can overlap on the GPU (other streams, other host
+ * threads on the same device) race and must be ordered by the caller.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  No device memory
+ * is allocated or freed by this call. */
+te_status te_quantize_fp8_dbias_noalloc(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                                        const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col,
+                                        float* amax_out, float* scale_inv_out, float* dbias, void* stream);
+
 /* ---- GEMMs ----------------------------------------------------------------------
  * Common: A [M, K], B [N, K] contraction-major; D [M, N] row-major of out_dtype
  * (TE_BF16, round-to-nearest-even, or TE_F32); bias (nullable) device fp32 [N];

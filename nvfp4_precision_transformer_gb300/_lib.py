@@ -42,6 +42,7 @@ SIGNATURES = {
     "te_scale_update": (_st, [ctypes.POINTER(te_recipe), _int, _int, _vp, _vp, _vp, _vp, _i64, _vp]),
     "te_quantize_fp8": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp]),
     "te_quantize_mxfp8": (_st, [_vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "te_quantize_fp8_dbias_noalloc": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "te_dbias_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "te_quantize_fp8_dbias": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]),
@@ -157,6 +158,15 @@ def te_quantize_fp8_dbias(x, fmt: int, dbias, workspace, scale=None, compute_sca
     _check("te_quantize_fp8_dbias", lib().te_quantize_fp8_dbias(
         _ptr(x), _in_dtype(x), r, c, fmt, _ptr(scale), compute_scale, _ptr(q_row), _ptr(q_col), _ptr(amax_out),
         _ptr(scale_inv_out), _ptr(dbias), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def te_quantize_fp8_dbias_noalloc(x, fmt: int, dbias, scale=None, compute_scale: int = 0, q_row=None, q_col=None,
+                                  amax_out=None, scale_inv_out=None, stream=None):
+    """te_quantize_fp8_dbias with the library's fixed scratch array instead of a workspace."""
+    r, c = _rc(x)
+    _check("te_quantize_fp8_dbias_noalloc", lib().te_quantize_fp8_dbias_noalloc(
+        _ptr(x), _in_dtype(x), r, c, fmt, _ptr(scale), compute_scale, _ptr(q_row), _ptr(q_col), _ptr(amax_out),
+        _ptr(scale_inv_out), _ptr(dbias), _stream(stream)))
 
 
 def te_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):

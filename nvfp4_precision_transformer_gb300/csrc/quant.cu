@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <type_traits>
 
 #include "common.cuh"
@@ -1150,3 +1152,52 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
 }
 
 }  // extern "C"
+
+// ---- allocation-free bias-gradient quantization --------------------------------------------------
+// Some callers cannot allocate device memory at the point where they quantize dY: code
+// that runs while a memory pool is locked or sized up front, or a host runtime that owns
+// every allocation and hands the library only the tensors it computes on.  For them the
+// workspace of te_quantize_fp8_dbias lives in this fixed array instead (4 MiB, one per
+// GPU that loads the library, held until the process exits).
+namespace {
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;
+static __device__ __align__(256) float g_dbias_scratch[kNoAllocScratchFloats];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device: host code sees only a
+// host-side stand-in for the array's name, so the address is looked up once per device,
+// with that device current, and kept.
+cudaError_t scratch_address(float** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[d] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dbias_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[d] = static_cast<float*>(p);
+  }
+  *out = g_scratch_ptr[d];
+  return cudaSuccess;
+}
+}  // namespace
+
+extern "C" te_status te_quantize_fp8_dbias_noalloc(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols,
+                                                   te_dtype fmt, const float* scale, int compute_scale, uint8_t* q_row,
+                                                   uint8_t* q_col, float* amax_out, float* scale_inv_out,
+                                                   float* dbias, void* stream) {
+  if (rows < 0 || cols < 0) return TE_ERR_SHAPE;
+  if (dbias != nullptr && te_dbias_workspace_bytes(rows, cols) > kNoAllocScratchFloats * sizeof(float))
+    return TE_ERR_SHAPE;  // more 64-row-tile partial sums than the fixed scratch holds
+  float* ws = nullptr;
+  if (dbias != nullptr && rows * cols > 0) {
+    const cudaError_t e = scratch_address(&ws);
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  return te_quantize_fp8_dbias(x, in_dtype, rows, cols, fmt, scale, compute_scale, q_row, q_col, amax_out,
+                               scale_inv_out, dbias, ws, kNoAllocScratchFloats * sizeof(float), stream);
+}
