@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--schedule-layers", type=int, default=24,
+                   help="layers of the DelayedScaling schedule measured eager and as CUDA graphs (0: skip)")
+    p.add_argument("--schedule-steps", type=int, default=4)
     return p.parse_args()
 
 
@@ -368,6 +371,10 @@ def main():
     # end to end through the C ABI from pinned host buffers (headline recipe)
     if not args.no_e2e and HEADLINE[0] in recipes:
         line["e2e"] = run_e2e(layer, args, ws)
+    if args.schedule_layers > 0:
+        del layer, tensors
+        torch.cuda.empty_cache()
+        line["schedule"] = run_schedule(args, cfg, dev, rank, ws)
     if rank == 0 and not args.no_cpu:
         elems = 2.0 * sum(cfg.tokens * ki + no * ki + cfg.tokens * no for _, ki, no in linears(cfg))
         ms, desc, secs = oracle_sample(256, args.hidden, cfg.tokens, lf, elems)
@@ -378,6 +385,59 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_schedule(args, cfg, dev, rank, ws):
+    """The 24-layer step under FP8 DelayedScaling (each tensor quantized once per step into
+    both copies, batched scale updates; X Student-t(3) with 0.1 % outliers x100, distinct
+    W per layer), timed eager and replayed as CUDA graphs (one per history slot)."""
+    import torch
+    from nvfp4_precision_transformer_gb300.linear import ScheduleGraphs, ScheduleStep
+    from nvfp4_precision_transformer_gb300.shapes import linears
+    from synthetic import gaussian, seed_for, student_t_outliers
+    import nvfp4_precision_transformer_gb300 as te
+    layers = []
+    for l in range(args.schedule_layers):
+        lin = []
+        for i, (_, k_in, n_out) in enumerate(linears(cfg)):
+            s = seed_for(5, 100 * l + i, 0) + 97 * rank
+            lin.append((student_t_outliers((cfg.tokens, k_in), s, device=dev),
+                        gaussian((n_out, k_in), 0.02, s + 1, device=dev),
+                        gaussian((cfg.tokens, n_out), 1e-3, s + 2, device=dev),
+                        gaussian((n_out,), 0.02, s + 3, dtype=torch.float32, device=dev)))
+        layers.append(lin)
+    sched = ScheduleStep(layers, history_len=16, device=dev)
+    flops = sched.gemm_flops()
+
+    def timed(run, first):
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = te.te_launch_count()
+        e0.record()
+        for t in range(first, first + args.schedule_steps):
+            run(t)
+        e1.record()
+        torch.cuda.synchronize()
+        return reduce_max(e0.elapsed_time(e1), ws) / args.schedule_steps, te.te_launch_count() - n0
+
+    for t in range(2):
+        sched.run(t)
+    eager_ms, eager_launches = timed(sched.run, 2)
+    graphs = ScheduleGraphs(sched)
+    graphs.run(2 + args.schedule_steps)
+    graph_ms, _ = timed(graphs.run, 3 + args.schedule_steps)
+    assert te.te_get_last_error() == 0, "device error in the schedule"
+    out = {"layers": args.schedule_layers, "recipe": "fp8_delayed (each tensor quantized once per step, both copies)",
+           "history_len": 16, "steps": args.schedule_steps,
+           "eager_ms_per_step": round(eager_ms, 3), "graph_ms_per_step": round(graph_ms, 3),
+           "eager_ms_per_layer": round(eager_ms / args.schedule_layers, 4),
+           "graph_ms_per_layer": round(graph_ms / args.schedule_layers, 4),
+           "gemm_tflops_graph": round(flops / (graph_ms * 1e-3) / 1e12, 1),
+           "launches_per_step": int(eager_launches // args.schedule_steps)}
+    del graphs, sched, layers
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(layer, args, ws):

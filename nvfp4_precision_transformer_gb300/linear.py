@@ -283,3 +283,85 @@ class HostStreamedLayer:
         if autocast and recipe == "fp8_delayed":
             with torch.cuda.stream(self.s_comp):
                 self.layer.scale_update()
+
+
+class ScheduleStep:
+    """A training step's worth of linears under DelayedScaling (the 24-layer schedule).
+
+    Per layer and linear, each tensor is quantized once per step into both copies (the
+    DelayedScaling cast records its amax in the same read), then the linear's Fprop, Dgrad
+    and Wgrad GEMMs run; after the last layer one batched scale update per direction
+    records the amaxes and refreshes every scale ("Introduction to FP8 training using
+    Transformer Engine": DelayedScaling with an amax history, HYBRID formats).  Quantized
+    copies and outputs are shared by the layers (each layer's are consumed before the next
+    layer overwrites them); inputs are per layer.  ``layers[l][i] = (x, w, dy, bias)``.
+    """
+
+    def __init__(self, layers, history_len: int = 16, device="cuda"):
+        import torch
+        self.layers = layers
+        n_lin = sum(len(lin) for lin in layers)
+        self.fwd = DelayedState(2 * n_lin, history_len, device)
+        self.bwd = DelayedState(n_lin, history_len, device)
+        self.recipe = L.te_recipe(L.E4M3, L.E5M2, history_len, L.ALGO_MAX, 0, 1)
+        self.history_len = history_len
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = torch.bfloat16
+        self.bufs = {}
+        for lin in layers:
+            for x, w, dy, _ in lin:
+                key = (x.shape[0], x.shape[1], w.shape[0])
+                if key in self.bufs:
+                    continue
+                M, K, N = key
+                self.bufs[key] = dict(xr=torch.empty(M, K, **u8), xc=torch.empty(K, M, **u8),
+                                      wr=torch.empty(N, K, **u8), wc=torch.empty(K, N, **u8),
+                                      dr=torch.empty(M, N, **u8), dc=torch.empty(N, M, **u8),
+                                      y=torch.empty(M, N, dtype=bf, device=device),
+                                      dx=torch.empty(M, K, dtype=bf, device=device),
+                                      dw=torch.empty(N, K, dtype=bf, device=device))
+
+    def run(self, step: int) -> None:
+        E4, E5 = L.E4M3, L.E5M2
+        k = 0
+        fs, fsi, fa = self.fwd.scale, self.fwd.scale_inv, self.fwd.amax
+        bs, bsi, ba = self.bwd.scale, self.bwd.scale_inv, self.bwd.amax
+        for lin in self.layers:
+            for x, w, dy, bias in lin:
+                b = self.bufs[(x.shape[0], x.shape[1], w.shape[0])]
+                ix, iw = 2 * k, 2 * k + 1
+                L.te_quantize_fp8(x, E4, fs[ix:ix + 1], 0, b["xr"], b["xc"], fa[ix:ix + 1])
+                L.te_quantize_fp8(w, E4, fs[iw:iw + 1], 0, b["wr"], b["wc"], fa[iw:iw + 1])
+                L.te_quantize_fp8(dy, E5, bs[k:k + 1], 0, b["dr"], b["dc"], ba[k:k + 1])
+                L.te_gemm_fp8(b["xr"], E4, b["wr"], E4, fsi[ix:ix + 1], fsi[iw:iw + 1], b["y"], bias)
+                L.te_gemm_fp8(b["dr"], E5, b["wc"], E4, bsi[k:k + 1], fsi[iw:iw + 1], b["dx"])
+                L.te_gemm_fp8(b["dc"], E5, b["xc"], E4, bsi[k:k + 1], fsi[ix:ix + 1], b["dw"])
+                k += 1
+        L.te_scale_update(self.recipe, 0, self.fwd.hist, fa, fs, fsi, step)
+        L.te_scale_update(self.recipe, 1, self.bwd.hist, ba, bs, bsi, step)
+
+    def gemm_flops(self) -> float:
+        return sum(6.0 * x.shape[0] * x.shape[1] * w.shape[0] for lin in self.layers for x, w, _, _ in lin)
+
+
+class ScheduleGraphs:
+    """CUDA-graph replay of a ``ScheduleStep``: one graph per history slot.
+
+    A step's launches differ only in the history slot its scale update writes (step mod
+    the history length, with the update interval 1 of the recipe), so one captured graph
+    per slot replays any step.  Capture after at least one eager step (first calls set
+    kernel attributes)."""
+
+    def __init__(self, sched: ScheduleStep):
+        import torch
+        self.sched = sched
+        self.graphs = []
+        stream = torch.cuda.Stream()
+        for slot in range(sched.history_len):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                sched.run(slot)
+            self.graphs.append(g)
+
+    def run(self, step: int) -> None:
+        self.graphs[step % self.sched.history_len].replay()
