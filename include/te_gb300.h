@@ -224,6 +224,23 @@ te_status te_quantize_fp8_dbias_noalloc(const void* x, te_dtype in_dtype, int64_
                                         const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col,
                                         float* amax_out, float* scale_inv_out, float* dbias, void* stream);
 
+/* LayerNorm fused with the FP8 cast of its output: the step before the QKV and MLP-up
+ * Fprop (te.LayerNorm / the fused LayerNorm kernels of "Introduction to FP8 training
+ * using Transformer Engine").  x bf16 [rows, cols] (cols % 16 == 0, cols <= 8192);
+ * gamma, beta device fp32 [cols] (16-byte aligned).  Per row: mu = mean, var = biased
+ * variance (fp32, fixed summation order), rsigma = 1 / sqrt(var + eps);
+ * y = ((x - mu) * rsigma) * gamma + beta in fp32, rounded to bf16 -- the LN output,
+ * written to ln_out (bf16 [rows, cols], nullable) -- and that bf16 value is cast to FP8
+ * as te_quantize_fp8 would cast it: q_row = sat(fl32(y * scale[0])) (fmt E4M3 / E5M2,
+ * DelayedScaling's scale from the history).  mu, rsigma (device fp32 [rows], nullable)
+ * are kept for the backward pass; amax_out (nullable) = max |y| over the bf16 outputs;
+ * scale_inv_out (nullable) = 1 / scale.  One read of x from HBM per row.  (The col copy
+ * for Wgrad comes from te_quantize_fp8 on ln_out.) */
+te_status te_layernorm_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, const float* gamma,
+                           const float* beta, float eps, te_dtype fmt, const float* scale, uint8_t* q_row,
+                           void* ln_out, float* mu, float* rsigma, float* amax_out, float* scale_inv_out,
+                           void* stream);
+
 /* ---- GEMMs ----------------------------------------------------------------------
  * Common: A [M, K], B [N, K] contraction-major; D [M, N] row-major of out_dtype
  * (TE_BF16, round-to-nearest-even, or TE_F32); bias (nullable) device fp32 [N];

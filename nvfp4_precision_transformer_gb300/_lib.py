@@ -42,6 +42,8 @@ SIGNATURES = {
     "te_scale_update": (_st, [ctypes.POINTER(te_recipe), _int, _int, _vp, _vp, _vp, _vp, _i64, _vp]),
     "te_quantize_fp8": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp]),
     "te_quantize_mxfp8": (_st, [_vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "te_layernorm_fp8": (_st, [_vp, _int, _i64, _i64, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _vp, _vp]),
     "te_quantize_fp8_dbias_noalloc": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "te_dbias_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "te_quantize_fp8_dbias": (_st, [_vp, _int, _i64, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -167,6 +169,14 @@ def te_quantize_fp8_dbias_noalloc(x, fmt: int, dbias, scale=None, compute_scale:
     _check("te_quantize_fp8_dbias_noalloc", lib().te_quantize_fp8_dbias_noalloc(
         _ptr(x), _in_dtype(x), r, c, fmt, _ptr(scale), compute_scale, _ptr(q_row), _ptr(q_col), _ptr(amax_out),
         _ptr(scale_inv_out), _ptr(dbias), _stream(stream)))
+
+
+def te_layernorm_fp8(x, gamma, beta, eps: float, fmt: int, scale, q_row, ln_out=None, mu=None, rsigma=None,
+                     amax_out=None, scale_inv_out=None, stream=None):
+    r, c = _rc(x)
+    _check("te_layernorm_fp8", lib().te_layernorm_fp8(
+        _ptr(x), _in_dtype(x), r, c, _ptr(gamma), _ptr(beta), float(eps), fmt, _ptr(scale), _ptr(q_row),
+        _ptr(ln_out), _ptr(mu), _ptr(rsigma), _ptr(amax_out), _ptr(scale_inv_out), _stream(stream)))
 
 
 def te_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):

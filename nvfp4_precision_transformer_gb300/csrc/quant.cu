@@ -332,6 +332,153 @@ __global__ void scale_update_kernel(int n, int L, int algo, int interval, float 
   scale_inv[i] = __fdiv_rn(1.0f, s);
 }
 
+// ---- LayerNorm fused with the FP8 cast of its output -----------------------------------------------
+// Persistent CTAs of up to 12 warps (two row buffers per warp must fit in shared memory);
+// each warp walks rows (grid-stride) with two shared-memory
+// row buffers: lane 0 bulk-copies the next row from HBM (one cp.async.bulk per row,
+// completion on the buffer's mbarrier) while the warp normalises the current one.
+// Mean and biased variance are fp32 (pairs of elements as packed fp32 operations, each an
+// IEEE round-to-nearest operation): each lane keeps one running sum per element position
+// of its 16-byte chunks (l, l + 32, ... in order), adds the 8 sums in position order, and
+// an xor-butterfly (offsets 16, 8, 4, 2, 1) combines the lanes;
+// rsigma = 1 / sqrt(var + eps) (both correctly rounded).  y = fl(fl(fl(x + (-mu)) * rsigma)
+// * gamma) + beta, rounded to bf16 (the LN output), and that bf16 value is cast:
+// q = sat(fl32(y_bf16 * scale)); the amax of the bf16 outputs is recorded for
+// DelayedScaling.
+constexpr int kLnWarps = 12;
+constexpr int64_t kLnMaxCols = 8192;
+
+__global__ void __launch_bounds__(32 * kLnWarps, 1)
+    layernorm_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t R, int64_t C, const float* __restrict__ gamma,
+                         const float* __restrict__ beta, float eps, int e5m2, const float* __restrict__ scale,
+                         uint8_t* __restrict__ q, __nv_bfloat16* __restrict__ ln_out, float* __restrict__ mu_out,
+                         float* __restrict__ rs_out, float* amax_out, int* err) {
+  extern __shared__ __align__(128) uint8_t ln_smem[];
+  __shared__ uint64_t ln_bar[kLnWarps][2];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);   // <= kLnWarps (fewer for long rows)
+  const int64_t nch = C / 8;
+  const uint32_t row_bytes = static_cast<uint32_t>(C * 2);
+  // gamma and beta once per CTA, then two row buffers per warp
+  float4* sg = reinterpret_cast<float4*>(ln_smem);
+  float4* sb = sg + C / 4;
+  uint8_t* rows_base = ln_smem + C * 8;
+  uint4* buf[2] = {reinterpret_cast<uint4*>(rows_base + (2 * wib) * row_bytes),
+                   reinterpret_cast<uint4*>(rows_base + (2 * wib + 1) * row_bytes)};
+  for (int64_t i = threadIdx.x; i < C / 4; i += blockDim.x) {
+    sg[i] = __ldg(reinterpret_cast<const float4*>(gamma) + i);
+    sb[i] = __ldg(reinterpret_cast<const float4*>(beta) + i);
+  }
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * nw + wib;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * nw;
+  if (lane == 0) {
+    dev::mbar_init(&ln_bar[wib][0], 1);
+    dev::mbar_init(&ln_bar[wib][1], 1);
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+  auto fetch = [&](int64_t row, int b) {
+    dev::mbar_expect_tx(&ln_bar[wib][b], row_bytes);
+    dev::bulk_load(buf[b], x + row * C, row_bytes, &ln_bar[wib][b]);
+  };
+  if (lane == 0 && first < R) fetch(first, 0);
+  int abort_flag = 0;
+  float lmax = 0.0f;
+  const float sc = *scale;
+  int k = 0;
+  for (int64_t row = first; row < R; row += stride, ++k) {
+    const int bsel = k & 1;
+    if (lane == 0 && row + stride < R) fetch(row + stride, bsel ^ 1);   // that buffer's previous row is done
+    // lane 0 waits for the row (bounded) and the warp follows its verdict together
+    int ok = 1;
+    if (lane == 0) ok = dev::mbar_wait(&ln_bar[wib][bsel], static_cast<uint32_t>(k >> 1) & 1u, &abort_flag, err);
+    __syncwarp();
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+    const uint4* srow = buf[bsel];
+    // per lane: 8 running sums (one per position in a chunk; pairs as packed fp32 adds),
+    // added in position order
+    float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    for (int64_t j = lane; j < nch; j += 32) {
+      const uint4 v = srow[j];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        acc[t] = __fadd2_rn(acc[t], make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u)));
+    }
+    float sum = acc[0].x;
+    sum = __fadd_rn(sum, acc[0].y);
+#pragma unroll
+    for (int t = 1; t < 4; ++t) sum = __fadd_rn(__fadd_rn(sum, acc[t].x), acc[t].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+    const float mu = __fdiv_rn(sum, static_cast<float>(C));
+    const float2 nmu = make_float2(-mu, -mu);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[t] = make_float2(0.f, 0.f);
+    for (int64_t j = lane; j < nch; j += 32) {
+      const uint4 v = srow[j];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 d = __fadd2_rn(make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u)), nmu);
+        acc[t] = __fadd2_rn(acc[t], __fmul2_rn(d, d));
+      }
+    }
+    float sq = acc[0].x;
+    sq = __fadd_rn(sq, acc[0].y);
+#pragma unroll
+    for (int t = 1; t < 4; ++t) sq = __fadd_rn(__fadd_rn(sq, acc[t].x), acc[t].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
+    const float var = __fdiv_rn(sq, static_cast<float>(C));
+    const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    if (lane == 0) {
+      if (mu_out) mu_out[row] = mu;
+      if (rs_out) rs_out[row] = rs;
+    }
+    const float2 rs2 = make_float2(rs, rs), sc2 = make_float2(sc, sc);
+    for (int64_t j = lane; j < nch; j += 32) {
+      const uint4 v = srow[j];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const float4 g0 = sg[2 * j], g1 = sg[2 * j + 1], b0 = sb[2 * j], b1 = sb[2 * j + 1];
+      const float2 gg[4] = {{g0.x, g0.y}, {g0.z, g0.w}, {g1.x, g1.y}, {g1.z, g1.w}};
+      const float2 bb[4] = {{b0.x, b0.y}, {b0.z, b0.w}, {b1.x, b1.y}, {b1.z, b1.w}};
+      uint32_t ob[4];
+      float2 a[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 e = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+        const float2 y = __fadd2_rn(__fmul2_rn(__fmul2_rn(__fadd2_rn(e, nmu), rs2), gg[t]), bb[t]);
+        const __nv_bfloat162 yb = __floats2bfloat162_rn(y.x, y.y);   // .x in the low half
+        const uint32_t bits = *reinterpret_cast<const uint32_t*>(&yb);
+        ob[t] = bits;
+        const float2 yv = make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xFFFF0000u));
+        lmax = fmaxf(lmax, fmaxf(fabsf(yv.x), fabsf(yv.y)));
+        a[t] = __fmul2_rn(yv, sc2);
+      }
+      if (ln_out) reinterpret_cast<uint4*>(ln_out + row * C)[j] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      uint32_t qw[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t lo = e5m2 ? cvt_e5m2x2(a[2 * t].x, a[2 * t].y) : cvt_e4m3x2(a[2 * t].x, a[2 * t].y);
+        const uint32_t hi = e5m2 ? cvt_e5m2x2(a[2 * t + 1].x, a[2 * t + 1].y) : cvt_e4m3x2(a[2 * t + 1].x, a[2 * t + 1].y);
+        qw[t] = lo | (hi << 16);
+      }
+      reinterpret_cast<uint2*>(q + row * C)[j] = make_uint2(qw[0], qw[1]);
+    }
+    __syncwarp();   // every lane is done with this buffer before lane 0 refills it
+  }
+  if (abort_flag && lane == 0) {
+    // bounded wait for this warp's copies still in flight before the CTA exits
+    int dummy = 0;
+    for (int kk = k; kk < k + 2; ++kk) {
+      const int64_t row = first + static_cast<int64_t>(kk) * stride;
+      if (row < R) dev::mbar_wait(&ln_bar[wib][kk & 1], static_cast<uint32_t>(kk >> 1) & 1u, &dummy, err);
+    }
+  }
+  if (amax_out != nullptr) block_max_to(lmax, amax_out);
+}
+
 // Bias gradient from the per-tile partial sums.  A CTA owns 32 columns; its 8 warps sum
 // the tile rows t = w, w + 8, w + 16, ... in order, then warp 0 adds the 8 partial
 // sums in warp order -- a fixed order, so the result does not depend on timing.
@@ -1085,6 +1232,56 @@ te_status te_quantize_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_
                           float* scale_inv_out, void* stream) {
   return te_quantize_fp8_dbias(x, in_dtype, rows, cols, fmt, scale, compute_scale, q_row, q_col, amax_out,
                                scale_inv_out, nullptr, nullptr, 0, stream);
+}
+
+te_status te_layernorm_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, const float* gamma,
+                           const float* beta, float eps, te_dtype fmt, const float* scale, uint8_t* q_row,
+                           void* ln_out, float* mu, float* rsigma, float* amax_out, float* scale_inv_out,
+                           void* stream) {
+  te_status s = check_2d(x, in_dtype, rows, cols);
+  if (s != TE_OK) return s;
+  if (in_dtype != TE_BF16 || (fmt != TE_E4M3 && fmt != TE_E5M2)) return TE_ERR_DTYPE;
+  if (cols % 16 != 0 || cols > kLnMaxCols) return TE_ERR_SHAPE;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return TE_ERR_ARG;
+  if (scale == nullptr || q_row == nullptr || gamma == nullptr || beta == nullptr) return TE_ERR_NULL;
+  if (!aligned16(q_row) || !aligned16(gamma) || !aligned16(beta) || (ln_out && !aligned16(ln_out)))
+    return TE_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess)
+    return record_cuda(cudaGetLastError());
+  if (rows > 0) {
+    // gamma, beta (8 B per column) and two bf16 row buffers per warp within 224 KB
+    const int64_t fit = (224 * 1024 - 8 * cols) / (4 * cols);
+    const int nw = static_cast<int>(fit < kLnWarps ? fit : kLnWarps);
+    const size_t smem = static_cast<size_t>(8 * cols) + static_cast<size_t>(2 * nw) * static_cast<size_t>(cols) * 2;
+    static bool attr_set[64] = {false};
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
+      if (cudaFuncSetAttribute(layernorm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 224 * 1024) !=
+          cudaSuccess)
+        return record_cuda(cudaGetLastError());
+      attr_set[dev_id] = true;
+    }
+    int* err = device_error_word();
+    if (err == nullptr) return record_cuda(cudaErrorInvalidDevice);
+    const int64_t want = (rows + nw - 1) / nw;
+    const unsigned grid = static_cast<unsigned>(want < num_sms() ? want : num_sms());
+    layernorm_fp8_kernel<<<grid, 32 * nw, smem, st>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, cols, gamma, beta, eps, fmt == TE_E5M2, scale, q_row,
+        static_cast<__nv_bfloat16*>(ln_out), mu, rsigma, amax_out, err);
+    count_launch();
+    s = launch_status();
+    if (s != TE_OK) return s;
+  }
+  if (scale_inv_out != nullptr) {
+    TileArgs a{};   // publishes 1 / scale through the quantizer's own path: an empty launch
+    a.scale = scale;
+    a.scale_inv_out = scale_inv_out;
+    a.fmax = fmt == TE_E4M3 ? 448.0f : 57344.0f;
+    s = launch_qtile_any<kQE4M3, false>(x, TE_BF16, 0, cols, nullptr, nullptr, a, st);
+  }
+  return s;
 }
 
 te_status te_quantize_mxfp8(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, uint8_t* q_row,

@@ -16,11 +16,12 @@ Modules
   philox    -- Philox4x32-10 counter-based generator (Salmon et al., SC'11)
   recipes   -- DelayedScaling and CurrentScaling scale updates
   quantize  -- per-tensor FP8, MXFP8 and NVFP4 quantizers (RHT, SR, 2D)
-  gemm      -- fp64 GEMM over dequantized operands, epilogue
+  gemm      -- fp64 GEMM over dequantized operands, epilogue, Wgrad accumulation
+  layernorm -- LayerNorm of the rows (the step before the QKV / MLP-up Fprop)
 
 Every function is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle_*``
 to a closed form, a brute-force check, a hand-worked table or an independent
 second implementation.  Parity status per function is listed in each module's
 docstring; none is unpinned.
 """
-from . import formats, philox, recipes, quantize, gemm  # noqa: F401
+from . import formats, philox, recipes, quantize, gemm, layernorm  # noqa: F401
