@@ -60,6 +60,9 @@ def parse():
     p.add_argument("--schedule-layers", type=int, default=24,
                    help="layers of the DelayedScaling schedule measured eager and as CUDA graphs (0: skip)")
     p.add_argument("--schedule-steps", type=int, default=4)
+    p.add_argument("--case", default="", help="time one kernel case instead of the layer (see KERNEL_CASES)")
+    p.add_argument("--shape", type=int, nargs="+", default=None, help="rows cols (quantizers) or M N K (GEMMs)")
+    p.add_argument("--iters", type=int, default=10)
     return p.parse_args()
 
 
@@ -250,11 +253,108 @@ def workload_config(args):
 
 # ---- our arm ---------------------------------------------------------------------------------------
 
+KERNEL_CASES = ("amax", "amax_rht", "fp8_row", "fp8_both", "fp8_col_dbias", "mxfp8_both", "nvfp4_rn_row",
+                "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "layernorm_fp8",
+                "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4")
+
+
+def run_case(args):
+    """One kernel on one shape, ``--iters`` back-to-back launches after one warm-up: the
+    per-kernel measurements (and the command the ncu summaries are taken with)."""
+    import torch
+    import nvfp4_precision_transformer_gb300 as te
+    from synthetic import gaussian, rht_sign_mask
+    assert args.case in KERNEL_CASES, f"--case one of {KERNEL_CASES}"
+    dev = torch.device("cuda", 0)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    f1 = lambda v=0.0: torch.full((1,), v, device=dev)
+    signs = rht_sign_mask(7)
+    if args.case.startswith("gemm"):
+        M, N, K = args.shape or (15872, 4096, 16384)
+        D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        if args.case == "gemm_bf16":
+            A, B = gaussian((M, K), 1.0, 1, device=dev), gaussian((N, K), 1.0, 2, device=dev)
+            fn = lambda: te.te_gemm_bf16(A, B, D)
+        elif args.case == "gemm_fp8":
+            A, B = torch.randint(0, 120, (M, K), **u8), torch.randint(0, 120, (N, K), **u8)
+            one = f1(1.0)
+            fn = lambda: te.te_gemm_fp8(A, te.E4M3, B, te.E4M3, one, one, D)
+        elif args.case == "gemm_mxfp8":
+            A, B = torch.randint(0, 120, (M, K), **u8), torch.randint(0, 120, (N, K), **u8)
+            sA = torch.full((te.te_scale_bytes(te.E8M0, M, K),), 127, **u8)
+            sB = torch.full((te.te_scale_bytes(te.E8M0, N, K),), 127, **u8)
+            fn = lambda: te.te_gemm_mxfp8(A, sA, B, sB, D)
+        else:
+            A, B = torch.randint(0, 256, (M, K // 2), **u8), torch.randint(0, 256, (N, K // 2), **u8)
+            sA = torch.full((te.te_scale_bytes(te.UE4M3, M, K),), 0x38, **u8)
+            sB = torch.full((te.te_scale_bytes(te.UE4M3, N, K),), 0x38, **u8)
+            one = f1(1.0)
+            fn = lambda: te.te_gemm_nvfp4(A, sA, one, B, sB, one, D)
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    else:
+        R, C = args.shape or (15872, 16384)
+        x = gaussian((R, C), 1e-3, 3, device=dev)
+        amax, amax_r, sinv = f1(), f1(), f1()
+        te.te_amax_reduce(x, amax, amax_r, signs)
+        n = R * C
+        qr, qc = torch.empty(R, C, **u8), torch.empty(C, R, **u8)
+        nr, nc = torch.empty(R, C // 2, **u8), torch.empty(C, R // 2, **u8)
+        snr = torch.empty(te.te_scale_bytes(te.UE4M3, R, C), **u8)
+        snc = torch.empty(te.te_scale_bytes(te.UE4M3, C, R), **u8)
+        smr = torch.empty(te.te_scale_bytes(te.E8M0, R, C), **u8)
+        smc = torch.empty(te.te_scale_bytes(te.E8M0, C, R), **u8)
+        gr, gc = f1(), f1()
+        scale = f1(2.0 ** 14)
+        RHT, SR, D2 = te.NVFP4_RHT_COL, te.NVFP4_SR, te.NVFP4_2D
+        nv = lambda flags, row, col: te.te_quantize_nvfp4(
+            x, flags, signs, 7, 3, amax, amax_r, *((nr, snr, gr) if row else (None, None, None)),
+            *((nc, snc, gc) if col else (None, None, None)))
+        cases = {
+            "amax": (lambda: te.te_amax_reduce(x, amax), 2 * n),
+            "amax_rht": (lambda: te.te_amax_reduce(x, amax, amax_r, signs), 2 * n),
+            "fp8_row": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, None, amax, sinv), 3 * n),
+            "fp8_both": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, qc, amax, sinv), 4 * n),
+            "mxfp8_both": (lambda: te.te_quantize_mxfp8(x, qr, smr, qc, smc), 2 * n + 2 * (n + n // 32)),
+            "nvfp4_rn_row": (lambda: nv(0, True, False), 2 * n + n // 2 + n // 16),
+            "nvfp4_rht_col": (lambda: nv(RHT, False, True), 2 * n + n // 2 + n // 16),
+            "nvfp4_sr_row": (lambda: nv(SR, True, False), 2 * n + n // 2 + n // 16),
+            "nvfp4_sr_rht_col": (lambda: nv(SR | RHT, False, True), 2 * n + n // 2 + n // 16),
+            "nvfp4_2d_both": (lambda: nv(D2, True, True), 2 * n + n + n // 8),
+        }
+        if args.case == "fp8_col_dbias":
+            db = torch.empty(C, device=dev)
+            wsp = torch.empty(te.te_dbias_workspace_bytes(R, C) // 4, device=dev)
+            cases["fp8_col_dbias"] = (lambda: te.te_quantize_fp8_dbias(x, te.E5M2, db, wsp, scale=scale, q_col=qc,
+                                                                      amax_out=amax, scale_inv_out=sinv), 3 * n)
+        if args.case == "layernorm_fp8":
+            g, b = torch.ones(C, device=dev), torch.zeros(C, device=dev)
+            cases["layernorm_fp8"] = (lambda: te.te_layernorm_fp8(x, g, b, 1e-5, te.E4M3, scale, qr), 3 * n)
+        fn, work = cases[args.case]
+        unit = "GB/s"
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert te.te_get_last_error() == 0
+    ms = e0.elapsed_time(e1) / args.iters
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"case": args.case, "shape": list(args.shape) if args.shape else None, "ms": round(ms, 4),
+                      "rate": round(rate, 1), "unit": unit,
+                      "work": "flops" if unit == "TFLOP/s" else "algorithmic bytes"}), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.case:
+        run_case(args)
         return
 
     import torch
