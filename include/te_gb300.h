@@ -105,7 +105,9 @@ enum {
  * amax_rht (nullable): max |y| where y is x's column-wise view transformed by
  * the 16-point random Hadamard transform along the rows (chunks of 16 rows,
  * signs from the low 16 bits of rht_signs; see te_quantize_nvfp4), taken in the
- * same read.  Both outputs are device fp32 scalars, overwritten (not max-ed).
+ * same read.  Both outputs are device fp32 scalars, overwritten (not max-ed); amax
+ * may be NULL when amax_rht is not (only the rotated amax, as the RHT col copy
+ * needs), TE_ERR_NULL when both are.
  * rows % 16 == 0, cols % 16 == 0; rows * cols may be 0 (amax = 0). */
 te_status te_amax_reduce(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols,
                          float* amax, float* amax_rht, uint32_t rht_signs, void* stream);

@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__
 // 8-byte patches with the next patch's loads in flight while it rotates the current
 // one; columns are rotated in pairs as packed fp32 values, and the 1/4 of the
 // transform is applied to the maximum (exact: scaling by 1/4 and rounding are monotone).
-template <typename T, int VB>
+template <typename T, int VB, bool PLAIN>
 __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                                float* amax, float* amax_rht, uint32_t signs) {
   using Vec = typename std::conditional<VB == 16, uint4, uint2>::type;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
           lo = __uint_as_float(raw_word(cur[r], 2 * k) ^ sg);
           hi = __uint_as_float(raw_word(cur[r], 2 * k + 1) ^ sg);
         }
-        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+        if (PLAIN) m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
         y[r] = make_float2(lo, hi);
       }
       hadamard16x2(y);
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
 #pragma unroll
     for (int r = 0; r < 16; ++r) cur[r] = nxt[r];
   }
-  block_max_to(m, amax);
+  if (PLAIN) block_max_to(m, amax);
   block_max_to(__fmul_rn(mr, 0.25f), amax_rht);
 }
 
@@ -1048,7 +1048,8 @@ inline te_status check_2d(const void* x, te_dtype in, int64_t rows, int64_t cols
 
 te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, float* amax, float* amax_rht,
                       uint32_t signs, cudaStream_t st) {
-  if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return record_cuda(cudaGetLastError());
+  if (amax != nullptr && cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess)
+    return record_cuda(cudaGetLastError());
   if (amax_rht != nullptr && cudaMemsetAsync(amax_rht, 0, sizeof(float), st) != cudaSuccess)
     return record_cuda(cudaGetLastError());
   if (rows * cols == 0) return TE_OK;
@@ -1056,12 +1057,21 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
     const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? kRhtAmaxVB / 2 : kRhtAmaxVB / 4));
     const int64_t want = (patches + kThreads - 1) / kThreads;
     const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
-    if (in == TE_BF16)
-      amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, amax,
-                                                                amax_rht, signs);
-    else
-      amax_rht_kernel<float, kRhtAmaxVB><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols, amax, amax_rht,
-                                                        signs);
+    if (in == TE_BF16) {
+      auto* p = static_cast<const __nv_bfloat16*>(x);
+      if (amax != nullptr)
+        amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB, true><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
+                                                                                    signs);
+      else
+        amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB, false><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
+                                                                                     signs);
+    } else {
+      auto* p = static_cast<const float*>(x);
+      if (amax != nullptr)
+        amax_rht_kernel<float, kRhtAmaxVB, true><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
+      else
+        amax_rht_kernel<float, kRhtAmaxVB, false><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht, signs);
+    }
   } else if (in == TE_BF16) {
     amax_kernel<__nv_bfloat16, false><<<patch_blocks(rows, cols, 16, 8), kThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), rows, cols, amax, nullptr, signs);
@@ -1147,7 +1157,7 @@ te_status te_amax_reduce(const void* x, te_dtype in_dtype, int64_t rows, int64_t
                          uint32_t rht_signs, void* stream) {
   te_status s = check_2d(x, in_dtype, rows, cols);
   if (s != TE_OK) return s;
-  if (amax == nullptr) return TE_ERR_NULL;
+  if (amax == nullptr && amax_rht == nullptr) return TE_ERR_NULL;
   return launch_amax(x, in_dtype, rows, cols, amax, amax_rht, rht_signs & 0xFFFFu, static_cast<cudaStream_t>(stream));
 }
 

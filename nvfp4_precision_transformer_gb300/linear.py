@@ -103,7 +103,8 @@ class QuantLinear:
 
     def _q_nv(self, name, t, flags, row=None, col=None, rotated=False):
         amax, amax_rht = self.namax[name]
-        L.te_amax_reduce(t, amax, amax_rht if rotated else None, self.rht_signs)
+        # a rotated col copy needs only the rotated amax
+        L.te_amax_reduce(t, None if rotated else amax, amax_rht if rotated else None, self.rht_signs)
         rq = row if row is not None else (None, None, None)
         cq = col if col is not None else (None, None, None)
         L.te_quantize_nvfp4(t, flags, self.rht_signs, self.sr_seed, self.sr_offset, amax, amax_rht,

@@ -274,6 +274,36 @@ def test_codonfm_attn_out_fprop_sampled(kind):
     G.check_no_device_error()
 
 
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+def test_codonfm_mlp_down_fprop_sampled(kind):
+    """The longest contraction of the layer: 15872 x 4096 x 16384 (MLP down, Fprop)."""
+    M, K, N = 15872, 16384, 4096
+    x = gaussian((M, K), 1.0, 801).to(G.DEV)
+    w = gaussian((N, K), 0.02, 802).to(G.DEV)
+    b = gaussian((N,), 0.02, 803, dtype=torch.float32).to(G.DEV)
+    rows, cols = _sample(M, 96, 5), _sample(N, 96, 6)
+    x32, w32 = G.f32_np(x), G.f32_np(w)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device=G.DEV)
+    if kind == "bf16":
+        te.te_gemm_bf16(x, w, D, b)
+        A64, B64 = x32[rows], w32[cols]
+    else:
+        xr, _, xs = _fp8_current(x, "e4m3")
+        wr, _, ws = _fp8_current(w, "e4m3")
+        te.te_gemm_fp8(xr, te.E4M3, wr, te.E4M3, xs, ws, D, b)
+        sx, six = Rc.current_scale(Q.amax(x32), "e4m3")
+        sw, siw = Rc.current_scale(Q.amax(w32), "e4m3")
+        A64 = Q.fp8_dequant(Q.fp8_cast(x32[rows], sx, "e4m3"), six, "e4m3")
+        B64 = Q.fp8_dequant(Q.fp8_cast(w32[cols], sw, "e4m3"), siw, "e4m3")
+    torch.cuda.synchronize()
+    got = G.f32_np(D)[np.ix_(rows, cols)].astype(np.float64)
+    ref = OG.gemm(A64, B64, bias=b.cpu().numpy()[cols])
+    exp = F.bf16_bits_to_f32(F.f64_to_bf16_bits(ref)).astype(np.float64)
+    err = OG.rel_frobenius(got, exp)
+    assert err <= TOL, f"{kind}: {err:.3e}"
+    G.check_no_device_error()
+
+
 @pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
 def test_codonfm_wgrad_sampled(kind):
     """dW = dY^T X for attention output: 4096 x 4096 x 15872 (contraction over tokens)."""

@@ -43,6 +43,11 @@ def test_amax_and_rht_amax(shape, dtype):
     assert ar == Q.amax(Q.rht16(np.ascontiguousarray(x32.T), signs))
     a2, _ = G.amax(x)
     assert a2 == a
+    # the rotated amax alone (plain amax pointer NULL)
+    ar_only = G.scalar(-1.0)
+    te.te_amax_reduce(x, None, ar_only, signs)
+    torch.cuda.synchronize()
+    assert np.float32(ar_only.item()) == ar
     G.check_no_device_error()
 
 
