@@ -253,7 +253,7 @@ def workload_config(args):
 
 # ---- our arm ---------------------------------------------------------------------------------------
 
-KERNEL_CASES = ("amax", "amax_rht", "fp8_row", "fp8_both", "fp8_col_dbias", "mxfp8_both", "nvfp4_rn_row",
+KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_both", "fp8_col_dbias", "mxfp8_both", "nvfp4_rn_row",
                 "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "layernorm_fp8",
                 "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4")
 
@@ -312,6 +312,7 @@ def run_case(args):
         cases = {
             "amax": (lambda: te.te_amax_reduce(x, amax), 2 * n),
             "amax_rht": (lambda: te.te_amax_reduce(x, amax, amax_r, signs), 2 * n),
+            "amax_rht_only": (lambda: te.te_amax_reduce(x, None, amax_r, signs), 2 * n),
             "fp8_row": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, None, amax, sinv), 3 * n),
             "fp8_both": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, qc, amax, sinv), 4 * n),
             "mxfp8_both": (lambda: te.te_quantize_mxfp8(x, qr, smr, qc, smc), 2 * n + 2 * (n + n // 32)),

@@ -65,20 +65,20 @@ __device__ __forceinline__ uint4 pack_fp8_16(const float (&v)[16], float s) {
 
 // ---- Philox4x32-10 (Salmon et al., SC'11) and stochastic E2M1 rounding ---------------
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10 with its ten round keys given (k0[i] = seed_lo + i * 0x9E3779B9,
+// k1[i] = seed_hi + i * 0xBB67AE85, the key schedule of the published definition): the
+// kernels read them from their parameters, so no key bumps execute per call.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&k0)[10], const uint32_t (&k1)[10]) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    if (i) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;  // one 32x32 -> 64-bit multiply each
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
     const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
-    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0[i], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1[i], static_cast<uint32_t>(p0));
   }
   return c;
 }
+
 
 // Four E2M1 codes with stochastic rounding (element i in bits 4i..4i+3).  The
 // hardware conversion adds 16 random bits below the kept bit and truncates; the
@@ -556,6 +556,7 @@ struct TileArgs {
   int64_t kpad_row, kpad_col;
   // NVFP4
   uint32_t flags, signs, seed_lo, seed_hi, off_lo, off_hi;
+  uint32_t rk0[10], rk1[10];   // Philox round keys of (seed_lo, seed_hi)
   const float* amax;
   const float* amax_rht;
   float* gdec_row;
@@ -633,7 +634,7 @@ __device__ __forceinline__ uint2 nv_pack16(const float* v, float r, const uint4&
 
 // Random words of the 16 elements g .. g + 15 (g a multiple of 16) of copy `copy_id`.
 __device__ __forceinline__ uint4 nv_rand(const TileArgs& a, uint64_t g, uint32_t copy_id) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(g >> 4), copy_id, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
+  return philox4x32_10_rk(make_uint4(static_cast<uint32_t>(g >> 4), copy_id, a.off_lo, a.off_hi), a.rk0, a.rk1);
 }
 
 template <int L>
@@ -1348,6 +1349,10 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
   a.signs = rht_signs & 0xFFFFu;
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  for (int i = 0; i < 10; ++i) {   // the Philox key schedule: bumped by the Weyl constants each round
+    a.rk0[i] = a.seed_lo + static_cast<uint32_t>(i) * 0x9E3779B9u;
+    a.rk1[i] = a.seed_hi + static_cast<uint32_t>(i) * 0xBB67AE85u;
+  }
   a.off_lo = static_cast<uint32_t>(offset);
   a.off_hi = static_cast<uint32_t>(offset >> 32);
   a.amax = amax;
