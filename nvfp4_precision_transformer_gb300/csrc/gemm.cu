@@ -486,8 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float b0 = args.bias ? __ldg(args.bias + nb + 2 * i) : 0.0f;
-              const float b1 = args.bias ? __ldg(args.bias + nb + 2 * i + 1) : 0.0f;
+              // N is a multiple of 16: the box's second half may lie past N (the store
+              // clips it), where the bias is not read
+              const bool bin = args.bias && nb + 2 * i < args.N;
+              const float b0 = bin ? __ldg(args.bias + nb + 2 * i) : 0.0f;
+              const float b1 = bin ? __ldg(args.bias + nb + 2 * i + 1) : 0.0f;
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmaf_rn(__uint_as_float(acc[bx][2 * i]), alpha, b0),
                                                               __fmaf_rn(__uint_as_float(acc[bx][2 * i + 1]), alpha, b1));
               w[i] = *reinterpret_cast<const uint32_t*>(&h2);
