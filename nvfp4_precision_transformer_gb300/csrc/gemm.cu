@@ -9,7 +9,7 @@
 // Every kind moves 32 bytes of each operand row per instruction, so one k-tile
 // is a 128-byte row slice (one 128-byte-swizzle atom) and 4 instructions.
 //
-// CTA = 11 warps, one CTA per SM (the shared-memory footprint guarantees it):
+// CTA = 11 warps (NVFP4 12), one CTA per SM (the shared-memory footprint guarantees it):
 //   warp 0      TMA producer: A tile [128 x 128 B], B tile and, for the block-scaled
 //               kinds, the scale-factor atoms, into a shared-memory ring guarded by
 //               full/empty mbarriers;
@@ -20,10 +20,11 @@
 //   warps 2-9   epilogue: each warp owns a 32-lane quarter of TMEM and a 128-column
 //               half of the 128 x 256 accumulator, drains it to registers, releases
 //               the accumulator, then applies alpha / bias, rounds and stores;
-//   warp 10     block-scaled kinds: issues the scale-factor copies (NVFP4 12, MXFP8 3 per
-//               k-tile) as soon as a stage lands and commits them onto the stage's
-//               sf_ready barrier, so the tensor pipe overlaps them with the MMAs of
-//               earlier k-tiles (copies and MMAs from one thread execute in issue order).
+//   warp 10(-11) block-scaled kinds: issue the scale-factor copies (NVFP4 12, MXFP8 3 per
+//               k-tile) as soon as a stage lands and commit them onto the stage's
+//               sf_ready barrier, so they run beside the MMAs of earlier k-tiles (copies
+//               and MMAs from one thread execute in issue order).  One thread's copies
+//               complete at about one per 46 ns, so NVFP4 splits its 12 between two warps.
 // Every kind runs as CTA pairs (2-CTA clusters, tcgen05 cta_group::2) on 256 x 256
 // tiles: each CTA stages 128 rows of A and 128 rows of B (BF16 / FP8 / MXFP8 6 stages,
 // NVFP4 5), the leader's thread issues M = 256 MMAs that read both CTAs' operands and
@@ -53,8 +54,7 @@ enum Kind { kBF16 = 0, kFP8 = 1, kMXFP8 = 2, kNVFP4 = 3 };
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kEpiWarps = 8;
-constexpr int kCopyWarp = 2 + kEpiWarps;               // scale-factor copier (block-scaled kinds)
-constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kCopyWarp = 2 + kEpiWarps;               // first scale-factor copier (block-scaled kinds)
 constexpr int kGroupM = 8;
 
 // CG = 1: one CTA per 128 x 256 tile.  CG = 2 (BF16 / FP8): a CTA pair per 256 x 256
@@ -71,6 +71,11 @@ struct Cfg {
   // The scale copies (NVFP4 12, MXFP8 3 per k-tile) go out from a warp of their own,
   // so the tensor pipe overlaps them with the MMAs (pairs: NVFP4 +12 %, MXFP8 +11 %).
   static constexpr bool kSfCopier = kBlockScaled;
+  // One thread's copies complete at about one per 46 ns whatever their size, so NVFP4's
+  // 12 per k-tile from one thread outlast the k-tile's MMAs: two copier warps, each
+  // issuing the copies of half the k-steps (+29 %).
+  static constexpr int kSfCopiers = KIND == kNVFP4 ? 2 : 1;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kSfCopiers);
   static constexpr uint32_t kTmemCols = 512u;
   static constexpr int kABytes = BM * 128;
   static constexpr int kBBytes = kBRows * 128;
@@ -125,7 +130,7 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 }
 
 template <int KIND, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSa,
                 const __grid_constant__ CUtensorMap tmSb, const __grid_constant__ GemmArgs args) {
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::mbar_init(&acc_empty[s], kEpiWarps * CG);
     }
     dev::mbar_init(drain, 1);
-    for (int st = 0; st < kStages; ++st) dev::mbar_init(&sf_ready[st], 1);
+    for (int st = 0; st < kStages; ++st) dev::mbar_init(&sf_ready[st], C::kSfCopiers);
     *abort_flag = 0;
     dev::fence_barrier_init();
     dev::prefetch_tmap(&tmA);
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   // Scale atoms of stage `st` (shared memory) -> its TMEM slot, one copy per 512-byte atom.
-  auto issue_sf_copies = [&](int st) {
+  auto issue_sf_copies = [&](int st, int jlo, int jhi) {
     const uint32_t sfa_t = tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
     const uint32_t sfb_t = sfa_t + C::kSfaCols;
     const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
@@ -206,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 #pragma unroll
     for (int j = 0; j < C::kSfAtoms; ++j) {
+      if (j < jlo || j >= jhi) continue;
       cp(sfa_t + 4 * j, sfa_s + 512 * j);
 #pragma unroll
       for (int h = 0; h < 2; ++h) cp(sfb_t + 8 * j + 4 * h, sfb_s + h * C::kSfAtoms * 512 + 512 * j);
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
-      auto copy_sf = [&](int st) { issue_sf_copies(st); };
+      auto copy_sf = [&](int st) { issue_sf_copies(st, 0, C::kSfAtoms); };
       for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
@@ -378,9 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int dummy = 0;
       dev::mbar_wait(drain, 0, &dummy, args.err);
     }
-  } else if (warp == kCopyWarp) {
-    // ------------------------------------------------ scale-factor copier (one thread; the pair's leader)
+  } else if (warp >= kCopyWarp) {
+    // ------------------------------------------------ scale-factor copiers (one thread each; the pair's leader)
+    const int copier = warp - kCopyWarp;
     if (C::kSfCopier && lane == 0 && leader) {
+      const int jlo = copier * C::kSfAtoms / C::kSfCopiers, jhi = (copier + 1) * C::kSfAtoms / C::kSfCopiers;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = !*abort_flag;
@@ -395,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           dev::tc_fence_after();
-          issue_sf_copies(stage);
+          issue_sf_copies(stage, jlo, jhi);
           if (kPair) dev::tc_commit_pair(&sf_ready[stage], 1);
           else dev::tc_commit(&sf_ready[stage]);
           last = stage;
@@ -547,7 +555,7 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemTotal;
   cfg.stream = st;
   cfg.attrs = attr;
