@@ -975,13 +975,17 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
   const int64_t n = ((a.R + 63) / 64) * tiles_c;
   const int64_t W = static_cast<int64_t>(gridDim.x) * kQWarps;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kQWarps + warp;
+  // Work item t covers tile n - 1 - t: the tensor is walked from its end backwards, so
+  // that the tiles an amax pass over the same tensor read last (forwards, just before
+  // this launch) are the first ones read here, while they are still in L2.
+  const int64_t last = n - 1;
   if (lane == 0) {
     for (int s = 0; s < kQStages; ++s) {
       const int64_t t = first + s * W;
       if (t < n) {
         dev::mbar_expect_tx(&bars[s], kQTileBytes);
-        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>((t % tiles_c) * 128),
-                         static_cast<int>((t / tiles_c) * 64));
+        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>(((last - t) % tiles_c) * 128),
+                         static_cast<int>(((last - t) / tiles_c) * 64));
       }
     }
   }
@@ -992,7 +996,7 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
     const int s = k % kQStages;
     const uint32_t ph = static_cast<uint32_t>(k / kQStages) & 1u;
     if (!dev::mbar_wait(&bars[s], ph, &abort_flag, a.err)) break;
-    const int64_t r0 = (t / tiles_c) * 64, c0 = (t % tiles_c) * TC;
+    const int64_t r0 = ((last - t) / tiles_c) * 64, c0 = ((last - t) % tiles_c) * TC;
     const uint8_t* tile = ring + s * kQTileBytes;
     if (lane == 0) dev::bulk_wait_read0();  // the previous tile's boxes have been read out
     __syncwarp();
@@ -1008,8 +1012,8 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
       const int64_t nt = t + kQStages * W;
       if (nt < n) {
         dev::mbar_expect_tx(&bars[s], kQTileBytes);
-        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>((nt % tiles_c) * 128),
-                         static_cast<int>((nt / tiles_c) * 64));
+        dev::tma_load_2d(ring + s * kQTileBytes, &tm_in, &bars[s], static_cast<int>(((last - nt) % tiles_c) * 128),
+                         static_cast<int>(((last - nt) / tiles_c) * 64));
       }
     }
   }
