@@ -40,8 +40,9 @@
 // The accumulator is double-buffered in TMEM for BF16/FP8 (2 x 256 columns); the
 // block-scaled kinds keep one 256-column accumulator plus a per-stage scale-factor
 // region and rely on the early release of the register drain for overlap.
-// Tiles are visited in a grouped raster (8 M-tiles per group) so concurrently
-// running CTAs share A and B tiles in L2.  No cluster multicast is used.
+// Tiles are visited in a grouped raster (16 pair M-tiles, 4096 rows, per group) so
+// concurrently running CTAs share A and B tiles in L2, and B is streamed from DRAM
+// once per group.  No cluster multicast is used.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -55,7 +56,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kEpiWarps = 8;
 constexpr int kCopyWarp = 2 + kEpiWarps;               // first scale-factor copier (block-scaled kinds)
-constexpr int kGroupM = 8;
+constexpr int kGroupM = 16;
 
 // CG = 1: one CTA per 128 x 256 tile.  CG = 2 (BF16 / FP8): a CTA pair per 256 x 256
 // tile with the pair-wide MMA (tcgen05 cta_group::2): each CTA holds 128 rows of A
