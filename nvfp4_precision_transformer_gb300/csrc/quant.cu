@@ -116,9 +116,10 @@ __device__ __forceinline__ float2 f2neg(float2 a) { return make_float2(-a.x, -a.
 // Butterflies h = 1, 2, 4, 8 of the 16-point Hadamard transform on two columns at
 // once (y[r] holds row r of both); the same operations in the same order as rht16
 // (a - b is computed as a + (-b), which is the same rounded result).
+template <int kLastH = 8>
 __device__ __forceinline__ void hadamard16x2(float2 (&y)[16]) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h <= kLastH; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if (i & h) continue;
@@ -294,9 +295,15 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
         if (PLAIN) m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
         y[r] = make_float2(lo, hi);
       }
-      hadamard16x2(y);
+      // Butterflies h = 1, 2, 4; the last one (h = 8) is folded into the maximum:
+      // max(|fl(a + b)|, |fl(a - b)|) = fl(|a| + |b|) exactly (one of the two sums is
+      // +-(|a| + |b|), the other is no larger, and rounding is symmetric and monotone).
+      hadamard16x2<4>(y);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) mr = fmaxf(mr, fmaxf(fabsf(y[r].x), fabsf(y[r].y)));
+      for (int r = 0; r < 8; ++r) {
+        mr = fmaxf(mr, __fadd_rn(fabsf(y[r].x), fabsf(y[r + 8].x)));
+        mr = fmaxf(mr, __fadd_rn(fabsf(y[r].y), fabsf(y[r + 8].y)));
+      }
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) cur[r] = nxt[r];
