@@ -312,11 +312,10 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
   block_max_to(__fmul_rn(mr, 0.25f), amax_rht);
 }
 
-// Vector width (bytes per patch row) of the rotated-amax kernel: 16 with the plain amax, 8 for
-// the rotated amax alone of bf16 input (there the 16-byte patches, double-buffered, need more
-// registers than two CTAs per SM leave and spill; the 8-byte ones run 8 % faster).
-constexpr int kRhtAmaxVB = 16;
-constexpr int kRhtOnlyVB = 8;
+// Vector width (bytes per patch row) of the rotated-amax kernel: 16-byte patches, double-
+// buffered, need more registers than two CTAs per SM leave and spill; the 8-byte ones do not
+// (rotated amax alone 8 % faster, with the plain amax the same).
+constexpr int kRhtAmaxVB = 8;
 
 // ---- DelayedScaling update ----------------------------------------------------------------------
 __global__ void scale_update_kernel(int n, int L, int algo, int interval, float fmax, float margin_mul,
@@ -1069,8 +1068,7 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
     return record_cuda(cudaGetLastError());
   if (rows * cols == 0) return TE_OK;
   if (amax_rht != nullptr) {
-    const int vb = (in == TE_BF16 && amax == nullptr) ? kRhtOnlyVB : kRhtAmaxVB;
-    const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? vb / 2 : vb / 4));
+    const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? kRhtAmaxVB / 2 : kRhtAmaxVB / 4));
     const int64_t want = (patches + kThreads - 1) / kThreads;
     const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
     if (in == TE_BF16) {
@@ -1079,7 +1077,7 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
         amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB, true><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
                                                                                     signs);
       else
-        amax_rht_kernel<__nv_bfloat16, kRhtOnlyVB, false><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
+        amax_rht_kernel<__nv_bfloat16, kRhtAmaxVB, false><<<grid, kThreads, 0, st>>>(p, rows, cols, amax, amax_rht,
                                                                                      signs);
     } else {
       auto* p = static_cast<const float*>(x);
