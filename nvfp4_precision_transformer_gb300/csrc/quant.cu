@@ -251,12 +251,13 @@ __global__ void __launch_bounds__(kThreads, 2) amax_kernel(const T* __restrict__
   block_max_to(p.absmax(), amax);
 }
 
-// Plain and rotated amax from one read.  Persistent grid: each thread walks 16-row x
-// 8-byte patches with the next patch's loads in flight while it rotates the current
-// one; columns are rotated in pairs as packed fp32 values, and the 1/4 of the
+// Plain and rotated amax from one read.  Persistent grid of 3 CTAs per SM: each thread
+// walks 16-row x 8-byte patches, loading one and rotating it (the other 23 warps' loads
+// fill the wait; a second patch in flight per thread, at 2 CTAs per SM, was 12-15 %
+// slower); columns are rotated in pairs as packed fp32 values, and the 1/4 of the
 // transform is applied to the maximum (exact: scaling by 1/4 and rounding are monotone).
 template <typename T, int VB, bool PLAIN>
-__global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kThreads, 3) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                                float* amax, float* amax_rht, uint32_t signs) {
   using Vec = typename std::conditional<VB == 16, uint4, uint2>::type;
   constexpr int PC = VB / sizeof(T);   // columns per patch
@@ -272,11 +273,10 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
       for (int r = 0; r < 16; ++r) raw[r] = __ldg(reinterpret_cast<const Vec*>(q + r * C));
     }
   };
-  Vec cur[16], nxt[16];
-  load(idx, cur);
+  Vec cur[16];
   float m = 0.0f, mr = 0.0f;
   for (; idx < total; idx += stride) {
-    load(idx + stride, nxt);
+    load(idx, cur);
 #pragma unroll
     for (int k = 0; k < PC / 2; ++k) {  // column pairs of the patch
       float2 y[16];
@@ -305,16 +305,13 @@ __global__ void __launch_bounds__(kThreads, 2) amax_rht_kernel(const T* __restri
         mr = fmaxf(mr, __fadd_rn(fabsf(y[r].y), fabsf(y[r + 8].y)));
       }
     }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) cur[r] = nxt[r];
   }
   if (PLAIN) block_max_to(m, amax);
   block_max_to(__fmul_rn(mr, 0.25f), amax_rht);
 }
 
-// Vector width (bytes per patch row) of the rotated-amax kernel: 16-byte patches, double-
-// buffered, need more registers than two CTAs per SM leave and spill; the 8-byte ones do not
-// (rotated amax alone 8 % faster, with the plain amax the same).
+// Vector width (bytes per patch row) of the rotated-amax kernel (16-byte patches need more
+// registers than three CTAs per SM leave).
 constexpr int kRhtAmaxVB = 8;
 
 // ---- DelayedScaling update ----------------------------------------------------------------------
@@ -1070,7 +1067,7 @@ te_status launch_amax(const void* x, te_dtype in, int64_t rows, int64_t cols, fl
   if (amax_rht != nullptr) {
     const int64_t patches = (rows / 16) * (cols / (in == TE_BF16 ? kRhtAmaxVB / 2 : kRhtAmaxVB / 4));
     const int64_t want = (patches + kThreads - 1) / kThreads;
-    const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
+    const unsigned grid = static_cast<unsigned>(want < 3 * num_sms() ? want : 3 * num_sms());
     if (in == TE_BF16) {
       auto* p = static_cast<const __nv_bfloat16*>(x);
       if (amax != nullptr)
