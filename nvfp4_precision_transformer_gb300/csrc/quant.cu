@@ -485,6 +485,122 @@ __global__ void __launch_bounds__(32 * kLnWarps, 1)
   if (amax_out != nullptr) block_max_to(lmax, amax_out);
 }
 
+// Rows of up to 4096 columns: the same arithmetic with each warp's row held in registers
+// (16-byte chunks lane, lane + 32, ...: at most 16 per lane) instead of shared-memory row
+// buffers, so that two CTAs of 8 warps fit an SM (16 warps, against 12 with row buffers);
+// gamma and beta stay in shared memory.  (A shared-memory buffer prefetching the next row
+// changed nothing: the three dependent passes, not the loads, set the pace.)
+constexpr int kLnRegCh = 16;
+constexpr int64_t kLnRegMaxCols = 32 * kLnRegCh * 8;
+
+__global__ void __launch_bounds__(256, 2)
+    layernorm_fp8_reg_kernel(const __nv_bfloat16* __restrict__ x, int64_t R, int64_t C, const float* __restrict__ gamma,
+                             const float* __restrict__ beta, float eps, int e5m2, const float* __restrict__ scale,
+                             uint8_t* __restrict__ q, __nv_bfloat16* __restrict__ ln_out, float* __restrict__ mu_out,
+                             float* __restrict__ rs_out, float* amax_out) {
+  extern __shared__ __align__(16) float4 ln_gb[];
+  float4* sg = ln_gb;
+  float4* sb = ln_gb + C / 4;
+  for (int64_t i = threadIdx.x; i < C / 4; i += blockDim.x) {
+    sg[i] = __ldg(reinterpret_cast<const float4*>(gamma) + i);
+    sb[i] = __ldg(reinterpret_cast<const float4*>(beta) + i);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const int64_t nch = C / 8;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * nw + wib;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * nw;
+  float lmax = 0.0f;
+  const float sc = *scale;
+  const float2 sc2 = make_float2(sc, sc);
+  for (int64_t row = first; row < R; row += stride) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * C);
+    uint4 v[kLnRegCh];
+#pragma unroll
+    for (int t = 0; t < kLnRegCh; ++t) {
+      const int64_t j = lane + 32 * t;
+      v[t] = j < nch ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // per lane: 8 running sums (one per position in a chunk; pairs as packed fp32 adds),
+    // added in position order; then an xor-butterfly over the lanes
+    float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int t = 0; t < kLnRegCh; ++t) {
+      if (lane + 32 * t >= nch) break;
+      const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        acc[k] = __fadd2_rn(acc[k], make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)));
+    }
+    float sum = acc[0].x;
+    sum = __fadd_rn(sum, acc[0].y);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) sum = __fadd_rn(__fadd_rn(sum, acc[k].x), acc[k].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+    const float mu = __fdiv_rn(sum, static_cast<float>(C));
+    const float2 nmu = make_float2(-mu, -mu);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < kLnRegCh; ++t) {
+      if (lane + 32 * t >= nch) break;
+      const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 d = __fadd2_rn(make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)), nmu);
+        acc[k] = __fadd2_rn(acc[k], __fmul2_rn(d, d));
+      }
+    }
+    float sq = acc[0].x;
+    sq = __fadd_rn(sq, acc[0].y);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) sq = __fadd_rn(__fadd_rn(sq, acc[k].x), acc[k].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
+    const float var = __fdiv_rn(sq, static_cast<float>(C));
+    const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    if (lane == 0) {
+      if (mu_out) mu_out[row] = mu;
+      if (rs_out) rs_out[row] = rs;
+    }
+    const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int t = 0; t < kLnRegCh; ++t) {
+      const int64_t j = lane + 32 * t;
+      if (j >= nch) break;
+      const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+      const float4 g0 = sg[2 * j], g1 = sg[2 * j + 1], b0 = sb[2 * j], b1 = sb[2 * j + 1];
+      const float2 gg[4] = {{g0.x, g0.y}, {g0.z, g0.w}, {g1.x, g1.y}, {g1.z, g1.w}};
+      const float2 bb[4] = {{b0.x, b0.y}, {b0.z, b0.w}, {b1.x, b1.y}, {b1.z, b1.w}};
+      uint32_t ob[4];
+      float2 a[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 e = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+        const float2 y = __fadd2_rn(__fmul2_rn(__fmul2_rn(__fadd2_rn(e, nmu), rs2), gg[k]), bb[k]);
+        const __nv_bfloat162 yb = __floats2bfloat162_rn(y.x, y.y);   // .x in the low half
+        const uint32_t bits = *reinterpret_cast<const uint32_t*>(&yb);
+        ob[k] = bits;
+        const float2 yv = make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xFFFF0000u));
+        lmax = fmaxf(lmax, fmaxf(fabsf(yv.x), fabsf(yv.y)));
+        a[k] = __fmul2_rn(yv, sc2);
+      }
+      if (ln_out) reinterpret_cast<uint4*>(ln_out + row * C)[j] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      uint32_t qw[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t lo = e5m2 ? cvt_e5m2x2(a[2 * k].x, a[2 * k].y) : cvt_e4m3x2(a[2 * k].x, a[2 * k].y);
+        const uint32_t hi = e5m2 ? cvt_e5m2x2(a[2 * k + 1].x, a[2 * k + 1].y) : cvt_e4m3x2(a[2 * k + 1].x, a[2 * k + 1].y);
+        qw[k] = lo | (hi << 16);
+      }
+      reinterpret_cast<uint2*>(q + row * C)[j] = make_uint2(qw[0], qw[1]);
+    }
+  }
+  if (amax_out != nullptr) block_max_to(lmax, amax_out);
+}
+
 // Bias gradient from the per-tile partial sums.  A CTA owns 32 columns; its 8 warps sum
 // the tile rows t = w, w + 8, w + 16, ... in order, then warp 0 adds the 8 partial
 // sums in warp order -- a fixed order, so the result does not depend on timing.
@@ -1270,7 +1386,16 @@ te_status te_layernorm_fp8(const void* x, te_dtype in_dtype, int64_t rows, int64
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (amax_out != nullptr && cudaMemsetAsync(amax_out, 0, sizeof(float), st) != cudaSuccess)
     return record_cuda(cudaGetLastError());
-  if (rows > 0) {
+  if (rows > 0 && cols <= kLnRegMaxCols) {
+    const int64_t want = (rows + 7) / 8;
+    const unsigned grid = static_cast<unsigned>(want < 2 * num_sms() ? want : 2 * num_sms());
+    layernorm_fp8_reg_kernel<<<grid, 256, static_cast<size_t>(8 * cols), st>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, cols, gamma, beta, eps, fmt == TE_E5M2, scale, q_row,
+        static_cast<__nv_bfloat16*>(ln_out), mu, rsigma, amax_out);
+    count_launch();
+    s = launch_status();
+    if (s != TE_OK) return s;
+  } else if (rows > 0) {
     // gamma, beta (8 B per column) and two bf16 row buffers per warp within 224 KB
     const int64_t fit = (224 * 1024 - 8 * cols) / (4 * cols);
     const int nw = static_cast<int>(fit < kLnWarps ? fit : kLnWarps);
