@@ -777,12 +777,13 @@ struct QGeom {
   static constexpr int COL_BOX = TC * COL_W;               // staging box bytes of the col copy
 };
 
-// Warps per CTA and input stages per warp (the same for every format: with the
-// hardware stochastic-rounding conversion no variant is arithmetic-bound enough to
-// prefer more warps over a second stage).
+// Warps per CTA and input stages per warp: 8 x 2 for FP8 / MXFP8; NVFP4, whose RHT, 2D and
+// stochastic-rounding paths are latency-bound, takes 11 warps (its smaller staging boxes
+// leave room): RHT col copy and 2D both copies 11-12 % faster, the RN row copy 2 % slower.
+// A third stage at fewer warps, or 12 warps with one stage, were slower.
 template <int FMT, bool SR>
 struct QLaunch {
-  static constexpr int NW = 8;
+  static constexpr int NW = FMT == kQNV ? 11 : 8;
   static constexpr int NS = 2;
 };
 template <typename T, int FMT, bool SR>
