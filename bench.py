@@ -62,7 +62,9 @@ def parse():
     p.add_argument("--schedule-steps", type=int, default=4)
     p.add_argument("--case", default="", help="time one kernel case instead of the layer (see KERNEL_CASES)")
     p.add_argument("--shape", type=int, nargs="+", default=None, help="rows cols (quantizers) or M N K (GEMMs)")
-    p.add_argument("--iters", type=int, default=10)
+    p.add_argument("--iters", type=int, default=50, help="--case: timed repetitions (median reported)")
+    p.add_argument("--case-warmup", type=int, default=None, help="--case: untimed launches first (10; 1 when --iters 1)")
+    p.add_argument("--no-flush", action="store_true", help="--case: do not evict L2 between repetitions")
     return p.parse_args()
 
 
@@ -259,8 +261,11 @@ KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_both", "fp8
 
 
 def run_case(args):
-    """One kernel on one shape, ``--iters`` back-to-back launches after one warm-up: the
-    per-kernel measurements (and the command the ncu summaries are taken with)."""
+    """One kernel on one shape: ``--case-warmup`` untimed launches, then ``--iters`` launches each
+    timed alone with CUDA events, L2 evicted between them by reading a 2x-L2 buffer outside the
+    timed events (reading, not writing, so that no dirty lines are written back during the next
+    launch), median reported: the per-kernel measurements (and, with ``--iters 1``, the command
+    the ncu summaries are taken with)."""
     import torch
     import nvfp4_precision_transformer_gb300 as te
     from synthetic import gaussian, rht_sign_mask
@@ -332,20 +337,32 @@ def run_case(args):
             cases["layernorm_fp8"] = (lambda: te.te_layernorm_fp8(x, g, b, 1e-5, te.E4M3, scale, qr), 3 * n)
         fn, work = cases[args.case]
         unit = "GB/s"
-    fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.iters):
+    warm = args.case_warmup if args.case_warmup is not None else (1 if args.iters == 1 else 10)
+    for _ in range(max(warm, 1)):
         fn()
-    e1.record()
+    torch.cuda.synchronize()
+    flush = None if args.no_flush or args.iters == 1 else torch.zeros(68 << 20, dtype=torch.float32, device=dev)
+    if flush is not None:
+        flush.sum()
+        torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.iters)]
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.sum()        # reads 272 MB > 2 x the 129 MB L2: nothing of the last launch stays cached
+        e0.record()
+        fn()
+        e1.record()
     torch.cuda.synchronize()
     assert te.te_get_last_error() == 0
-    ms = e0.elapsed_time(e1) / args.iters
+    times = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+    ms = times[len(times) // 2]
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     print(json.dumps({"case": args.case, "shape": list(args.shape) if args.shape else None, "ms": round(ms, 4),
                       "rate": round(rate, 1), "unit": unit,
-                      "work": "flops" if unit == "TFLOP/s" else "algorithmic bytes"}), flush=True)
+                      "work": "flops" if unit == "TFLOP/s" else "algorithmic bytes",
+                      "timing": {"reps": args.iters, "warmup": max(warm, 1), "stat": "median",
+                                 "min_ms": round(times[0], 4), "max_ms": round(times[-1], 4),
+                                 "l2": "evicted between reps" if flush is not None else "not evicted"}}), flush=True)
 
 
 def main():
