@@ -65,6 +65,7 @@ def parse():
     p.add_argument("--iters", type=int, default=50, help="--case: timed repetitions (median reported)")
     p.add_argument("--case-warmup", type=int, default=None, help="--case: untimed launches first (10; 1 when --iters 1)")
     p.add_argument("--no-flush", action="store_true", help="--case: do not evict L2 between repetitions")
+    p.add_argument("--layer-shapes", action="store_true", help="--case (GEMMs): time all 12 GEMM shapes of the layer")
     return p.parse_args()
 
 
@@ -167,56 +168,182 @@ def peaks():
 # ---- DRAM traffic of the dominant kernel (from a committed ncu summary) ---------------------------
 
 def fp8_gemm_traffic():
-    """DRAM bytes per FP8 GEMM launch measured by ncu for the current gemm.cu, else None.
+    """DRAM bytes per FP8 GEMM launch (mean over the layer's 12 shapes) from the committed ncu
+    figures (``profiles/gemm_fp8_dram_traffic_codonfm_layer.json``), else None.
 
-    The summary records the sha256 prefix of the source it was measured on; a
-    changed kernel reports no traffic until it is measured again."""
+    The figures record the sha256 prefix of the GEMM source they were measured on; a changed
+    kernel reports no traffic until it is measured again."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "gemm_fp8_dram_traffic_codonfm_layer.md")
+    prof = os.path.join(ROOT, "profiles", "gemm_fp8_dram_traffic_codonfm_layer.json")
     csrc = os.path.join(ROOT, "nvfp4_precision_transformer_gb300", "csrc")
     try:
-        fields = dict(line.split(":", 1) for line in open(prof) if line.count(":") == 1 and not line.startswith(("-", "#", " ")))
+        d = json.load(open(prof))
         h = hashlib.sha256()
         for name in ("gemm.cu", "common.cuh"):
             h.update(open(os.path.join(csrc, name), "rb").read())
-        if fields.get("kernel_source_sha256_prefix", "").strip() != h.hexdigest()[:16]:
-            return None, None
-        return int(fields["traffic_bytes_per_launch"]), int(fields["algorithmic_bytes_per_launch"])
+        if d.get("kernel_source_sha256_prefix") != h.hexdigest()[:16]:
+            return None, d.get("algorithmic_bytes_per_launch"), "GEMM source changed since the ncu capture"
+        return int(d["traffic_bytes_per_launch"]), int(d["algorithmic_bytes_per_launch"]), d.get("how")
     except (OSError, KeyError, ValueError):
-        return None, None
+        return None, None, "no ncu traffic figures committed"
 
 
 # ---- CPU oracle baseline ---------------------------------------------------------------------------
+#
+# The oracle (numpy, as it stands) on the host cores.  Its quantizers are row-independent
+# once the tensor's amax / scale is known, so rows are split over a pool of worker processes
+# (started with "spawn": the parent has already used the GPU); the fp64 GEMMs run in the
+# parent on the BLAS threads.  Both arms time the same sample: the attention-output linear
+# (4096 -> 4096) at SAMPLE_TOKENS tokens under FP8 CurrentScaling autocast (amax, row and col
+# copies of X, W and dY; Fprop, Dgrad and Wgrad in fp64).  The per-layer figure is
+# extrapolated from it per quantized element and per GEMM flop, and labelled so.
 
-def oracle_sample(tokens_sample: int, hidden: int, cfg_tokens: int, layer_flops: float, layer_elems: float):
-    """Time the oracle (as it stands) on FP8 CurrentScaling autocast Fprop of the attention-output
-    linear restricted to ``tokens_sample`` tokens: amax of X and W, FP8 quantization of the X slab
-    and of W, fp64 GEMM + bias.  Returns (ms per layer extrapolated, description, seconds)."""
+SAMPLE_TOKENS = 1024
+_POOL = None
+
+
+def _pool_init():
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+
+
+def oracle_pool():
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        _POOL = mp.get_context("spawn").Pool(cpu_threads(), initializer=_pool_init)
+    return _POOL
+
+
+def close_pool():
+    global _POOL
+    if _POOL is not None:
+        _POOL.terminate()
+        _POOL.join()
+        _POOL = None
+
+
+def _oracle_job(job):
+    """One row slab of one oracle quantizer (runs in a pool worker); returns a small checksum."""
+    from oracle import quantize as Q
+    kind, arr = job[0], job[1]
+    if kind == "amax":
+        return float(Q.amax(arr))
+    if kind == "rht_amax":
+        return float(Q.amax(Q.rht16(arr, job[2])))
+    if kind == "fp8":
+        return int(Q.fp8_cast(arr, job[2], job[3])[:1].sum())
+    if kind == "mx":
+        return int(Q.mxfp8_quantize(arr)[1][:1].sum())
+    if kind == "nv":
+        z = Q.rht16(arr, job[3]) if job[3] is not None else arr
+        return int(Q.nvfp4_quantize(z, job[2])[1][:1].sum())
+    raise ValueError(kind)
+
+
+def _pmap(kind, arr, *extra):
+    """Run one oracle quantizer over ``arr`` [R, C] in row slabs on the pool."""
+    import numpy as np
+    n = max(1, min(arr.shape[0] // 16, 2 * cpu_threads()))
+    bounds = np.linspace(0, arr.shape[0] // 16, n + 1).astype(int) * 16   # whole 16-row groups
+    jobs = [(kind, np.ascontiguousarray(arr[a:b]), *extra) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    return oracle_pool().map(_oracle_job, jobs)
+
+
+def oracle_linear_sample(hidden: int, layer_flops: float, layer_elems: float):
+    """FP8 CurrentScaling autocast of the attention-output linear at SAMPLE_TOKENS tokens by the
+    oracle.  Returns (ms per layer extrapolated, measured sample seconds, description)."""
     import numpy as np
     from oracle import gemm as OG, quantize as Q, recipes as Rc
     from oracle.formats import bf16_bits_to_f32
     from synthetic import gaussian, bf16_bits
-    x = bf16_bits_to_f32(bf16_bits(gaussian((tokens_sample, hidden), 1.0, 901)))
+    T = SAMPLE_TOKENS
+    x = bf16_bits_to_f32(bf16_bits(gaussian((T, hidden), 1.0, 901)))
     w = bf16_bits_to_f32(bf16_bits(gaussian((hidden, hidden), 0.02, 902)))
-    b = np.zeros(hidden, np.float32)
+    dy = bf16_bits_to_f32(bf16_bits(gaussian((T, hidden), 1e-3, 903)))
+    oracle_pool()
     t0 = time.perf_counter()
-    sx, ix = Rc.current_scale(Q.amax(x), "e4m3")
-    sw, iw = Rc.current_scale(Q.amax(w), "e4m3")
-    qx = Q.fp8_cast(x, sx, "e4m3")
-    qw = Q.fp8_cast(w, sw, "e4m3")
+    deq = {}
+    for name, t, fmt in (("x", x, "e4m3"), ("w", w, "e4m3"), ("dy", dy, "e5m2")):
+        amax = np.float32(max(_pmap("amax", t)))
+        s, si = Rc.current_scale(amax, fmt)
+        _pmap("fp8", t, s, fmt)                                   # row copy
+        _pmap("fp8", np.ascontiguousarray(t.T), s, fmt)           # col copy
+        deq[name] = (s, si, fmt)
     t1 = time.perf_counter()
-    OG.gemm(Q.fp8_dequant(qx, ix, "e4m3"), Q.fp8_dequant(qw, iw, "e4m3"), bias=b)
+    # the GEMMs consume the dequantized copies (the casts are repeated here for the operands,
+    # outside the timed quantizer region)
+    op = {k: Q.fp8_dequant(Q.fp8_cast(v, deq[k][0], deq[k][2]), deq[k][1], deq[k][2])
+          for k, v in (("x", x), ("w", w), ("dy", dy))}
     t2 = time.perf_counter()
-    q_per_elem = (t1 - t0) / (x.size + w.size)
-    g_per_flop = (t2 - t1) / (2.0 * tokens_sample * hidden * hidden)
-    ms = 1e3 * (q_per_elem * layer_elems + g_per_flop * layer_flops)
-    desc = (f"oracle FP8-current Fprop of attn_out on {tokens_sample} tokens x {hidden} (+ W {hidden}x{hidden}); "
-            f"extrapolated per element quantized ({layer_elems:.3g}/layer) and per GEMM flop ({layer_flops:.3g}/layer)")
-    return ms, desc, t2 - t0
+    OG.gemm(op["x"], op["w"])                 # Fprop  Y  = X W^T
+    OG.gemm(op["dy"], op["w"].T)              # Dgrad  dX = dY W
+    OG.gemm(op["dy"].T, op["x"].T)            # Wgrad  dW = dY^T X
+    t3 = time.perf_counter()
+    elems = 2.0 * (x.size + w.size + dy.size)
+    flops = 3 * 2.0 * T * hidden * hidden
+    ms = 1e3 * ((t1 - t0) / elems * layer_elems + (t3 - t2) / flops * layer_flops)
+    desc = (f"oracle FP8-current autocast of the attn-out linear at {T} tokens (X {T}x{hidden}, W {hidden}x{hidden}, "
+            f"dY {T}x{hidden}: amax + row + col copies on {cpu_threads()} pool processes, Fprop/Dgrad/Wgrad fp64 on the "
+            f"BLAS threads); per-layer value EXTRAPOLATED per quantized element ({layer_elems:.3g}/layer) and per "
+            f"GEMM flop ({layer_flops:.3g}/layer)")
+    return ms, (t1 - t0) + (t3 - t2), desc, {"quantize_s": round(t1 - t0, 3), "gemm_s": round(t3 - t2, 3),
+                                             "gemm_gflops": round(flops / (t3 - t2) / 1e9, 2)}
+
+
+def oracle_full_quantizers(tokens: int, hidden: int):
+    """The oracle's quantizers on one full CodonFM activation X [tokens, hidden] (bf16 N(0,1)):
+    FP8 CurrentScaling (amax, row + col), MXFP8 (row + col), NVFP4 (amax + rotated amax, RN
+    row, RHT col).  Wall ms on the pool and the algorithmic GB/s the GPU kernels are held to."""
+    import numpy as np
+    from oracle import quantize as Q, recipes as Rc
+    from oracle.formats import bf16_bits_to_f32
+    from synthetic import gaussian, bf16_bits, rht_sign_mask
+    x = bf16_bits_to_f32(bf16_bits(gaussian((tokens, hidden), 1.0, 904)))
+    xt = np.ascontiguousarray(x.T)
+    n = x.size
+    signs = rht_sign_mask(7)
+    oracle_pool()
+    out = {}
+
+    def timed(name, fn, bytes_):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        out[name] = {"ms": round(1e3 * dt, 1), "gbs": round(bytes_ / dt / 1e9, 4)}
+
+    def fp8():
+        s, _ = Rc.current_scale(np.float32(max(_pmap("amax", x))), "e4m3")
+        _pmap("fp8", x, s, "e4m3")
+        _pmap("fp8", xt, s, "e4m3")
+
+    def mx():
+        _pmap("mx", x)
+        _pmap("mx", xt)
+
+    def nv():
+        a = np.float32(max(_pmap("amax", x)))
+        ar = np.float32(max(_pmap("rht_amax", xt, signs)))
+        _pmap("nv", x, a, None)
+        _pmap("nv", xt, ar, signs)
+
+    timed("fp8_current_row_col", fp8, 6 * n)
+    timed("mxfp8_row_col", mx, 2 * n + 2 * (n + n / 32))
+    timed("nvfp4_row_rn_col_rht", nv, 2 * n + 2 * n + 2 * (n / 2 + n / 16))
+    out["tensor"] = f"X [{tokens}, {hidden}] bf16"
+    return out
 
 
 def cpu_threads():
     return os.cpu_count() or 1
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads") or 0) for i in threadpool_info()) or None
+    except Exception:
+        return os.environ.get("OPENBLAS_NUM_THREADS") or "library default (all cores)"
 
 
 # ---- reference arm -------------------------------------------------------------------------------
@@ -228,19 +355,24 @@ def run_reference(args, ws, rank):
     cfg = LayerConfig(hidden=args.hidden, intermediate=args.ffn, micro_batch=1, seq_len=args.tokens)
     lf = float(layer_flops(cfg))
     elems = 2.0 * sum(cfg.tokens * ki + no * ki + cfg.tokens * no for _, ki, no in linears(cfg))
-    times = []
-    desc = ""
+    est, secs = [], []
+    desc, parts = "", {}
     for i in range(args.warmup + args.steps):
-        ms, desc, _ = oracle_sample(64, args.hidden, cfg.tokens, lf, elems)
+        ms, s, desc, parts = oracle_linear_sample(args.hidden, lf, elems)
         if i >= args.warmup:
-            times.append(ms)
-    v = statistics.median(times)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "ms/layer", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            est.append(ms)
+            secs.append(s)
+    v = statistics.median(est)
+    sample_ms = 1e3 * statistics.median(secs)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "ms/layer", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sample_ms, 1),
+            "step": f"one oracle sample (measured): {desc}", "value_is": "extrapolated from the measured sample",
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(args),
-            "cpu_baseline": {"value": v, "unit": "ms/layer", "cores": cpu_threads(), "kind": "oracle", "sample": desc},
-            "e2e": {"value": v, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": round(v, 1), "unit": "ms/layer", "cores": cpu_threads(),
+                             "blas_threads": blas_threads(), "kind": "oracle", "sample": desc,
+                             "sample_seconds": round(sample_ms / 1e3, 3), "extrapolated": True, **parts},
+            "e2e": {"value": round(v, 1), "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -257,7 +389,8 @@ def workload_config(args):
 
 KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_both", "fp8_col_dbias", "mxfp8_both", "nvfp4_rn_row",
                 "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "layernorm_fp8",
-                "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4")
+                "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4",
+                "cublaslt_bf16", "cublaslt_fp8", "cublaslt_mxfp8", "cublaslt_nvfp4")
 
 
 def run_case(args):
@@ -274,7 +407,32 @@ def run_case(args):
     u8 = dict(dtype=torch.uint8, device=dev)
     f1 = lambda v=0.0: torch.full((1,), v, device=dev)
     signs = rht_sign_mask(7)
-    if args.case.startswith("gemm"):
+    if args.case.startswith("cublaslt"):
+        # context only: the same operand bytes through torch's cuBLASLt path (torch._scaled_mm /
+        # torch.matmul), never on the library's path
+        M, N, K = args.shape or (15872, 4096, 16384)
+        if args.case == "cublaslt_bf16":
+            A, B = gaussian((M, K), 1.0, 1, device=dev), gaussian((N, K), 1.0, 2, device=dev)
+            fn = lambda: torch.matmul(A, B.t())
+        else:
+            one = torch.ones((), device=dev)
+            if args.case == "cublaslt_fp8":
+                A = torch.randint(0, 120, (M, K), **u8).view(torch.float8_e4m3fn)
+                B = torch.randint(0, 120, (N, K), **u8).view(torch.float8_e4m3fn)
+                sa, sb = one, one
+            elif args.case == "cublaslt_mxfp8":
+                A = torch.randint(0, 120, (M, K), **u8).view(torch.float8_e4m3fn)
+                B = torch.randint(0, 120, (N, K), **u8).view(torch.float8_e4m3fn)
+                sa = torch.full((te.te_scale_bytes(te.E8M0, M, K),), 127, **u8).view(torch.float8_e8m0fnu)
+                sb = torch.full((te.te_scale_bytes(te.E8M0, N, K),), 127, **u8).view(torch.float8_e8m0fnu)
+            else:
+                A = torch.randint(0, 256, (M, K // 2), **u8).view(torch.float4_e2m1fn_x2)
+                B = torch.randint(0, 256, (N, K // 2), **u8).view(torch.float4_e2m1fn_x2)
+                sa = torch.full((te.te_scale_bytes(te.UE4M3, M, K),), 0x38, **u8).view(torch.float8_e4m3fn)
+                sb = torch.full((te.te_scale_bytes(te.UE4M3, N, K),), 0x38, **u8).view(torch.float8_e4m3fn)
+            fn = lambda: torch._scaled_mm(A, B.t(), sa, sb, out_dtype=torch.bfloat16)
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif args.case.startswith("gemm"):
         M, N, K = args.shape or (15872, 4096, 16384)
         D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         if args.case == "gemm_bf16":
@@ -350,14 +508,22 @@ def run_case(args):
         if flush is not None:
             flush.sum()        # reads 272 MB > 2 x the 129 MB L2: nothing of the last launch stays cached
         e0.record()
+        torch.cuda.nvtx.range_push("timed")     # ncu captures select the timed launches by this range
         fn()
+        torch.cuda.nvtx.range_pop()
         e1.record()
     torch.cuda.synchronize()
     assert te.te_get_last_error() == 0
     times = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+    if args.case.startswith("cublaslt"):
+        te_launches = "library (cuBLASLt via torch), context only"
+    else:
+        te_launches = "libte_gb300"
     ms = times[len(times) // 2]
     rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
-    print(json.dumps({"case": args.case, "shape": list(args.shape) if args.shape else None, "ms": round(ms, 4),
+    print(json.dumps({"case": args.case, "impl": te_launches, "gemm": getattr(args, "label", None),
+                      "shape": list(args.shape) if args.shape else None,
+                      "ms": round(ms, 4),
                       "rate": round(rate, 1), "unit": unit,
                       "work": "flops" if unit == "TFLOP/s" else "algorithmic bytes",
                       "timing": {"reps": args.iters, "warmup": max(warm, 1), "stat": "median",
@@ -365,14 +531,55 @@ def run_case(args):
                                  "l2": "evicted between reps" if flush is not None else "not evicted"}}), flush=True)
 
 
+PER_GEMM_FIELDS = ["recipe", "mode", "linear", "pass", "M", "N", "K", "ms", "tflops", "frac_of_peak"]
+
+
+def per_gemm_table(per_g, pk):
+    """One row per (recipe, mode, linear, pass): mean CUDA-event ms of that GEMM launch over the
+    timed steps, its TFLOP/s and the fraction of the recipe's tensor peak (measured bf16
+    sustained x the nominal dtype ratio).  Rows as lists under ``fields``."""
+    rows = []
+    for (r, m, lname, p, M, N, K), ts in per_g.items():
+        ms = statistics.mean(ts)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops_sustained"] * PEAK_RATIO[RECIPE_DTYPE[r]]
+        rows.append([r, m, lname, p, M, N, K, round(ms, 4), round(tf, 1), round(tf / peak, 4)])
+    return {"fields": PER_GEMM_FIELDS, "rows": rows,
+            "timing": "CUDA events around each GEMM launch inside the timed steps (quantizers excluded), mean"}
+
+
+def nvfp4_over_bf16(per):
+    """The pages' NVFP4-over-BF16 speed-ups: autocast (quantizers included) and kernel-only
+    (pre-quantized NVFP4 GEMMs against the BF16 GEMMs)."""
+    b = per.get("bf16/autocast")
+    na, npq = per.get("nvfp4/autocast"), per.get("nvfp4/prequant")
+    if not b or not na or not npq:
+        return None
+    return {"autocast": round(b["ms_per_layer"] / na["ms_per_layer"], 3),
+            "prequant_kernel_only": round(b["gemm_ms_per_layer"] / npq["gemm_ms_per_layer"], 3),
+            "pages_b300": {"autocast": 1.98, "prequant_kernel_only": 3.48}}
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
-        run_reference(args, ws, rank)
+        try:
+            run_reference(args, ws, rank)
+        finally:
+            close_pool()
         return
     if args.case:
-        run_case(args)
+        if args.layer_shapes:
+            # every GEMM shape of the layer, one JSON line each (GEMM cases only)
+            from nvfp4_precision_transformer_gb300.shapes import LayerConfig, layer_gemms
+            cfg = LayerConfig(hidden=args.hidden, intermediate=args.ffn, micro_batch=1, seq_len=args.tokens)
+            for g in layer_gemms(cfg):
+                args.shape = [g.M, g.N, g.K]
+                args.label = f"{g.linear}/{g.pass_}"
+                run_case(args)
+        else:
+            run_case(args)
         return
 
     import torch
@@ -413,7 +620,7 @@ def main():
                 ev = torch.cuda.Event(enable_timing=True)
                 ev.record()
                 if phase == 0:
-                    _g.append([lin.gemm_shape(p), ev, None])
+                    _g.append([lin.gemm_shape(p), ev, None, (lin.name, p)])
                 else:
                     _g[-1][2] = ev
             e0.record()
@@ -446,15 +653,18 @@ def main():
     total_ms = reduce_max(t_start.elapsed_time(t_end), ws)
     clocks = clk.summary()
 
-    # per recipe / mode aggregation
+    # per recipe / mode aggregation, and per GEMM (recipe, mode, linear, pass)
     pk = peaks()
     agg = {}
+    per_g = {}
     for r, m, e0, e1, gemms in records:
         d = agg.setdefault((r, m), {"seg": [], "gemm_ms": 0.0, "gemm_flops": 0.0})
         d["seg"].append(e0.elapsed_time(e1))
-        for (M, N, K), g0, g1 in gemms:
-            d["gemm_ms"] += g0.elapsed_time(g1)
+        for (M, N, K), g0, g1, (lname, p) in gemms:
+            t = g0.elapsed_time(g1)
+            d["gemm_ms"] += t
             d["gemm_flops"] += 2.0 * M * N * K
+            per_g.setdefault((r, m, lname, p, M, N, K), []).append(t)
     per = {}
     for (r, m), d in agg.items():
         ms = statistics.mean(d["seg"])
@@ -466,25 +676,28 @@ def main():
                            "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_peak": round(gemm_tflops / peak, 4),
                            "peak_tflops": round(peak, 1),
                            "pages_ms_b300": PAGES_MS.get((r, m))}
+    per_gemm = per_gemm_table(per_g, pk)
+    ratios = nvfp4_over_bf16(per)
     head = per.get(f"{HEADLINE[0]}/{HEADLINE[1]}") or next(iter(per.values()))
-    head_ms = reduce_max(head["ms_per_layer"], ws) / ws          # whole job: ws replicas in parallel
+    head_ms = reduce_max(head["ms_per_layer"], ws)     # per replica: the slowest rank's ms per layer
     # dominant kernel of the headline: the FP8 GEMM
     hd = agg.get(HEADLINE) or next(iter(agg.values()))
     fp8_peak = pk["bf16_tflops_sustained"] * PEAK_RATIO["fp8"]
     achieved = hd["gemm_flops"] / (hd["gemm_ms"] * 1e-3) / 1e12
-    traffic, alg_bytes = fp8_gemm_traffic()
+    traffic, alg_bytes, traffic_note = fp8_gemm_traffic()
     roofline = {"kernel": "gemm_kernel<FP8> (tcgen05 kind::f8f6f4)", "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "traffic": traffic, "algorithmic_bytes": alg_bytes,
+                "traffic": traffic, "algorithmic_bytes": alg_bytes, "traffic_note": traffic_note,
                 "flops_per_launch": round(hd["gemm_flops"] / (12 * args.steps)),
                 "peak_note": f"{pk['source']} bf16 sustained {pk['bf16_tflops_sustained']} x 2 (nominal FP8/BF16 ratio)",
                 "launches_per_layer": 12}
-
     line = {"metric": METRIC, "value": round(head_ms, 4), "unit": "ms/layer", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": round(head_ms / PAGES_MS[HEADLINE], 4), "dtype": "fp8",
-            "data": "synthetic", "config": workload_config(args), "per_recipe": per, "roofline": roofline,
-            "gpu_launches": int(launches), "clocks": clocks}
+            "data": "synthetic", "config": workload_config(args), "per_recipe": per, "per_gemm": per_gemm,
+            "nvfp4_over_bf16": ratios, "roofline": roofline, "gpu_launches": int(launches), "clocks": clocks,
+            "aggregate": {"layers_per_s": round(ws * 1e3 / head_ms, 3), "replicas": ws,
+                          "note": "value is ms per layer of one replica (max over ranks); replicas run in parallel"}}
 
     # end to end through the C ABI from pinned host buffers (headline recipe)
     if not args.no_e2e and HEADLINE[0] in recipes:
@@ -495,9 +708,12 @@ def main():
         line["schedule"] = run_schedule(args, cfg, dev, rank, ws)
     if rank == 0 and not args.no_cpu:
         elems = 2.0 * sum(cfg.tokens * ki + no * ki + cfg.tokens * no for _, ki, no in linears(cfg))
-        ms, desc, secs = oracle_sample(256, args.hidden, cfg.tokens, lf, elems)
-        line["cpu_baseline"] = {"value": round(ms, 1), "unit": "ms/layer", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": desc, "sample_seconds": round(secs, 2)}
+        ms, secs, desc, parts = oracle_linear_sample(args.hidden, lf, elems)
+        line["cpu_baseline"] = {"value": round(ms, 1), "unit": "ms/layer", "cores": cpu_threads(),
+                                "blas_threads": blas_threads(), "kind": "oracle", "sample": desc,
+                                "sample_seconds": round(secs, 3), "extrapolated": True, **parts,
+                                "full_tensor_quantizers": oracle_full_quantizers(cfg.tokens, args.hidden)}
+    close_pool()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -545,15 +761,33 @@ def run_schedule(args, cfg, dev, rank, ws):
     graphs = ScheduleGraphs(sched)
     graphs.run(2 + args.schedule_steps)
     graph_ms, _ = timed(graphs.run, 3 + args.schedule_steps)
+    del graphs
+    # the same step with the long amax history (NeMo's fp8_amax_history_len 1024): eager, the
+    # per-slot graphs would be 1024 captures
+    long_h = ScheduleStep(layers, history_len=1024, device=dev)
+    for t in range(2):
+        long_h.run(t)
+    long_ms, _ = timed(long_h.run, 2)
+    del long_h
+    # the BF16 GEMM path on the same tensors, alongside
+    bf = ScheduleStep(layers, device=dev, recipe="bf16")
+    bf.run(0)
+    bf_ms, _ = timed(bf.run, 1)
+    del bf
     assert te.te_get_last_error() == 0, "device error in the schedule"
-    out = {"layers": args.schedule_layers, "recipe": "fp8_delayed (each tensor quantized once per step, both copies)",
+    L = args.schedule_layers
+    out = {"layers": L, "recipe": "fp8_delayed (each tensor quantized once per step, both copies)",
            "history_len": 16, "steps": args.schedule_steps,
            "eager_ms_per_step": round(eager_ms, 3), "graph_ms_per_step": round(graph_ms, 3),
-           "eager_ms_per_layer": round(eager_ms / args.schedule_layers, 4),
-           "graph_ms_per_layer": round(graph_ms / args.schedule_layers, 4),
+           "eager_ms_per_layer": round(eager_ms / L, 4),
+           "graph_ms_per_layer": round(graph_ms / L, 4),
            "gemm_tflops_graph": round(flops / (graph_ms * 1e-3) / 1e12, 1),
-           "launches_per_step": int(eager_launches // args.schedule_steps)}
-    del graphs, sched, layers
+           "launches_per_step": int(eager_launches // args.schedule_steps),
+           "history_len_1024": {"eager_ms_per_step": round(long_ms, 3), "eager_ms_per_layer": round(long_ms / L, 4)},
+           "bf16": {"eager_ms_per_step": round(bf_ms, 3), "eager_ms_per_layer": round(bf_ms / L, 4),
+                    "gemm_tflops": round(flops / (bf_ms * 1e-3) / 1e12, 1),
+                    "fp8_delayed_speedup_graph": round(bf_ms / graph_ms, 3)}}
+    del sched, layers
     torch.cuda.empty_cache()
     return out
 
@@ -587,7 +821,7 @@ def run_e2e(layer, args, ws):
         main_s.wait_stream(s)
     e1.record(main_s)
     torch.cuda.synchronize()
-    ms = reduce_max(e0.elapsed_time(e1), ws) / args.e2e_steps / ws
+    ms = reduce_max(e0.elapsed_time(e1), ws) / args.e2e_steps      # per replica (max over ranks)
     return {"value": round(ms, 4), "unit": "ms/layer", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "recipe": HEADLINE[0], "steps": args.e2e_steps,
             "overlap": "per-linear input / output copies on their own streams overlap the compute"}

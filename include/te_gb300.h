@@ -120,6 +120,8 @@ te_status te_amax_reduce(const void* x, te_dtype in_dtype, int64_t rows, int64_t
  * amax[i] (most recent); if a is finite and > 0 and the new scale
  * s = fl32(fl32(fmax / a) * 2^-margin) is finite, scale[i] = s;
  * scale_inv[i] = fl32(1 / scale[i]).  fmax = 448 (E4M3) or 57344 (E5M2).
+ * A NaN amax is recorded like any other; the maximum over a window that holds
+ * it is NaN, so the scale is held while it stays in the window (as for +Inf).
  * ("Introduction to FP8 training using Transformer Engine", section
  * "FP8 Training について": one scaling factor per tensor, refreshed every step.)
  * Initial state expected from the caller: hist = 0, scale = scale_inv = 1.
@@ -220,8 +222,10 @@ te_status te_quantize_nvfp4(const void* x, te_dtype in_dtype, int64_t rows, int6
  * every call shares it: calls that can overlap on the GPU (other streams, other host
  * threads on the same device) race and must be ordered by the caller.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  No device memory
- * is allocated or freed by this call. */
+ * device current); make that first call before any stream capture.  The address is
+ * kept for the life of the process, so a device that the library has used must not be
+ * reset (cudaDeviceReset) while the library stays loaded.  Argument checks run before
+ * that lookup.  No device memory is allocated or freed by this call. */
 te_status te_quantize_fp8_dbias_noalloc(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
                                         const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col,
                                         float* amax_out, float* scale_inv_out, float* dbias, void* stream);

@@ -326,8 +326,13 @@ __global__ void scale_update_kernel(int n, int L, int algo, int interval, float 
   if ((step + 1) % interval != 0) return;
   float eff = a;
   if (algo == TE_ALGO_MAX) {
+    // a NaN anywhere in the window makes the maximum NaN (fmaxf would drop it), so the
+    // scale is held until the NaN leaves the window, as for an infinite amax
     eff = h[0];
-    for (int j = 1; j < L; ++j) eff = fmaxf(eff, h[j]);
+    for (int j = 1; j < L; ++j) {
+      const float v = h[j];
+      eff = (v > eff || isnan(v)) ? v : eff;
+    }
   }
   float s = scale[i];
   if (isfinite(eff) && eff > 0.0f) {
@@ -1336,16 +1341,32 @@ size_t te_dbias_workspace_bytes(int64_t rows, int64_t cols) {
   return static_cast<size_t>((rows + 63) / 64) * static_cast<size_t>(cols) * sizeof(float);
 }
 
-te_status te_quantize_fp8_dbias(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
-                                const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col, float* amax_out,
-                                float* scale_inv_out, float* dbias, float* workspace, size_t workspace_bytes,
-                                void* stream) {
+}  // extern "C"
+
+namespace {
+// Host-side checks of the per-tensor FP8 cast's arguments (everything but the dbias workspace).
+te_status check_fp8_cast(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                         const float* scale, int compute_scale, const uint8_t* q_row, const uint8_t* q_col,
+                         const float* amax_out, const float* dbias) {
   te_status s = check_2d(x, in_dtype, rows, cols);
   if (s != TE_OK) return s;
   if (fmt != TE_E4M3 && fmt != TE_E5M2) return TE_ERR_DTYPE;
   if (compute_scale != 0 && compute_scale != 1) return TE_ERR_ARG;
   if (compute_scale ? amax_out == nullptr : scale == nullptr) return TE_ERR_NULL;
   if ((q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col))) return TE_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(dbias) & 3u) return TE_ERR_ALIGN;
+  return TE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+te_status te_quantize_fp8_dbias(const void* x, te_dtype in_dtype, int64_t rows, int64_t cols, te_dtype fmt,
+                                const float* scale, int compute_scale, uint8_t* q_row, uint8_t* q_col, float* amax_out,
+                                float* scale_inv_out, float* dbias, float* workspace, size_t workspace_bytes,
+                                void* stream) {
+  te_status s = check_fp8_cast(x, in_dtype, rows, cols, fmt, scale, compute_scale, q_row, q_col, amax_out, dbias);
+  if (s != TE_OK) return s;
   const bool want_dbias = dbias != nullptr;
   if (want_dbias && cols > 0) {
     if (rows > 0 && workspace == nullptr) return TE_ERR_NULL;
@@ -1565,7 +1586,10 @@ extern "C" te_status te_quantize_fp8_dbias_noalloc(const void* x, te_dtype in_dt
                                                    te_dtype fmt, const float* scale, int compute_scale, uint8_t* q_row,
                                                    uint8_t* q_col, float* amax_out, float* scale_inv_out,
                                                    float* dbias, void* stream) {
-  if (rows < 0 || cols < 0) return TE_ERR_SHAPE;
+  // every argument check runs before the scratch address is looked up (that lookup may
+  // initialise the device context), so a bad call returns its TE_ERR_* and touches nothing
+  te_status s = check_fp8_cast(x, in_dtype, rows, cols, fmt, scale, compute_scale, q_row, q_col, amax_out, dbias);
+  if (s != TE_OK) return s;
   if (dbias != nullptr && te_dbias_workspace_bytes(rows, cols) > kNoAllocScratchFloats * sizeof(float))
     return TE_ERR_SHAPE;  // more 64-row-tile partial sums than the fixed scratch holds
   float* ws = nullptr;

@@ -27,6 +27,7 @@ from . import _lib as L
 
 RECIPES = ("bf16", "fp8_delayed", "fp8_current", "mxfp8", "nvfp4")
 PASSES = ("fprop", "dgrad", "wgrad")
+LAYER_LINEARS = ("qkv", "attn_out", "mlp_up", "mlp_down")
 
 
 class DelayedState:
@@ -54,6 +55,7 @@ class QuantLinear:
         M, Kin = x.shape
         Nout = w.shape[0]
         self.M, self.Kin, self.Nout = M, Kin, Nout
+        self.name = "linear"
         self.rht_signs, self.sr_seed, self.sr_offset = rht_signs, sr_seed, 0
         bf = torch.bfloat16
         self.y = torch.empty(M, Nout, dtype=bf, device=dev)
@@ -198,7 +200,7 @@ class Layer:
     """The four linears of one transformer layer with shared DelayedScaling state."""
 
     def __init__(self, tensors, recipes=RECIPES, history_len: int = 16, rht_signs: int = 0, sr_seed: int = 0,
-                 device="cuda"):
+                 device="cuda", names=None):
         n = len(tensors)
         self.recipes = recipes
         self.fwd = DelayedState(2 * n, history_len, device)
@@ -206,6 +208,9 @@ class Layer:
         self.recipe = L.te_recipe(L.E4M3, L.E5M2, history_len, L.ALGO_MAX, 0, 1)
         self.linears = [QuantLinear(x, w, dy, b, recipes, rht_signs, sr_seed, self.fwd, (2 * i, 2 * i + 1),
                                     self.bwd, i) for i, (x, w, dy, b) in enumerate(tensors)]
+        default = LAYER_LINEARS if n == len(LAYER_LINEARS) else tuple(f"linear{i}" for i in range(n))
+        for lin, name in zip(self.linears, names or default):
+            lin.name = name
         self.step_idx = 0
 
     def scale_update(self) -> None:
@@ -298,9 +303,11 @@ class ScheduleStep:
     layer overwrites them); inputs are per layer.  ``layers[l][i] = (x, w, dy, bias)``.
     """
 
-    def __init__(self, layers, history_len: int = 16, device="cuda"):
+    def __init__(self, layers, history_len: int = 16, device="cuda", recipe: str = "fp8_delayed"):
         import torch
+        assert recipe in ("fp8_delayed", "bf16"), recipe
         self.layers = layers
+        self.kind = recipe
         n_lin = sum(len(lin) for lin in layers)
         self.fwd = DelayedState(2 * n_lin, history_len, device)
         self.bwd = DelayedState(n_lin, history_len, device)
@@ -315,14 +322,17 @@ class ScheduleStep:
                 if key in self.bufs:
                     continue
                 M, K, N = key
-                self.bufs[key] = dict(xr=torch.empty(M, K, **u8), xc=torch.empty(K, M, **u8),
-                                      wr=torch.empty(N, K, **u8), wc=torch.empty(K, N, **u8),
-                                      dr=torch.empty(M, N, **u8), dc=torch.empty(N, M, **u8),
-                                      y=torch.empty(M, N, dtype=bf, device=device),
+                self.bufs[key] = dict(y=torch.empty(M, N, dtype=bf, device=device),
                                       dx=torch.empty(M, K, dtype=bf, device=device),
                                       dw=torch.empty(N, K, dtype=bf, device=device))
+                if recipe == "fp8_delayed":
+                    self.bufs[key].update(xr=torch.empty(M, K, **u8), xc=torch.empty(K, M, **u8),
+                                          wr=torch.empty(N, K, **u8), wc=torch.empty(K, N, **u8),
+                                          dr=torch.empty(M, N, **u8), dc=torch.empty(N, M, **u8))
 
     def run(self, step: int) -> None:
+        if self.kind == "bf16":
+            return self._run_bf16()
         E4, E5 = L.E4M3, L.E5M2
         k = 0
         fs, fsi, fa = self.fwd.scale, self.fwd.scale_inv, self.fwd.amax
@@ -340,6 +350,16 @@ class ScheduleStep:
                 k += 1
         L.te_scale_update(self.recipe, 0, self.fwd.hist, fa, fs, fsi, step)
         L.te_scale_update(self.recipe, 1, self.bwd.hist, ba, bs, bsi, step)
+
+    def _run_bf16(self) -> None:
+        """The same GEMMs in BF16 on the unquantized tensors (no scaling state)."""
+        KM, MN = L.K_MAJOR, L.MN_MAJOR
+        for lin in self.layers:
+            for x, w, dy, bias in lin:
+                b = self.bufs[(x.shape[0], x.shape[1], w.shape[0])]
+                L.te_gemm_bf16(x, w, b["y"], bias, KM, KM)
+                L.te_gemm_bf16(dy, w, b["dx"], None, KM, MN)
+                L.te_gemm_bf16(dy, x, b["dw"], None, MN, MN)
 
     def gemm_flops(self) -> float:
         return sum(6.0 * x.shape[0] * x.shape[1] * w.shape[0] for lin in self.layers for x, w, _, _ in lin)

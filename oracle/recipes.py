@@ -15,7 +15,7 @@ with a scale derived from past amaxes; CurrentScaling from the tensor's own
 amax ("How to Optimize Transformer-Based Models for Low-Precision Training",
 section "autocast モードの使用と事前量子化の比較").
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * initial state: history all zeros, scale 1, scale_inv 1;
   * step t quantizes with the current scale, then records its amax a_t into
     slot t mod L, then (if (t+1) mod interval == 0) recomputes the scale;

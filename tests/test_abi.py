@@ -71,6 +71,17 @@ def test_validation_before_any_device_work(lib):
     assert lib.te_gemm_bf16(fake, 0, fake, 0, None, fake, L.F32, 2, 32, 32, 32, None) == 8
     # empty GEMM is a no-op success
     assert lib.te_gemm_bf16(None, 0, None, 0, None, None, L.BF16, 0, 0, 32, 32, None) == 0
+    # the allocation-free dbias quantization validates before it looks anything up on a device
+    assert lib.te_quantize_fp8_dbias_noalloc(fake, L.BF16, 24, 32, L.E5M2, fake, 0, None, fake, None, None,
+                                             fake, None) == 2
+    assert lib.te_quantize_fp8_dbias_noalloc(fake, L.BF16, 32, 32, L.E2M1, fake, 0, None, fake, None, None,
+                                             fake, None) == 4
+    assert lib.te_quantize_fp8_dbias_noalloc(fake, L.BF16, 32, 32, L.E5M2, None, 0, None, fake, None, None,
+                                             fake, None) == 1
+    assert lib.te_quantize_fp8_dbias_noalloc(fake, L.BF16, 32, 32, L.E5M2, fake, 0, None, fake, None, None,
+                                             ctypes.c_void_p(0x1002), None) == 3
+    assert lib.te_quantize_fp8_dbias_noalloc(fake, L.BF16, 15872, 16384, L.E5M2, fake, 0, None, fake, None, None,
+                                             fake, None) == 2     # more partial sums than the fixed array holds
     # recipe validation
     r = L.te_recipe(L.E4M3, L.E5M2, 0, 0, 0, 1)
     assert lib.te_scale_update(ctypes.byref(r), 0, 4, fake, fake, fake, fake, 0, None) == 8

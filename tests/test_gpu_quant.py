@@ -80,6 +80,7 @@ def test_scale_update_matches_oracle(L, algo, margin, interval, bwd):
     amaxes = (rng.standard_exponential((steps, n)) * np.exp2(rng.integers(-20, 20, size=(steps, n)))).astype(np.float32)
     amaxes[3, :5] = 0.0
     amaxes[6, 7] = np.inf
+    amaxes[9, 11] = np.nan          # a NaN amax holds the scale while it is in the window (like Inf)
     recipe = te.te_recipe(te.E4M3, te.E5M2, L, algo, margin, interval)
     hist = torch.zeros(n * L, dtype=torch.float32, device=G.DEV)
     scale = torch.ones(n, dtype=torch.float32, device=G.DEV)

@@ -268,6 +268,113 @@ def test_sr_unbiased(v):
         assert abs(sub.mean() - np.float32(v)) < 4 * sigma * 2 + (hi - lo) * 2.0 ** -16
 
 
+# ---- stochastic rounding: fairness of the reading of a group's random word ----------------
+#
+# The rule reads one 32-bit word per group of four elements and gives each position a 16-bit
+# value R.  What makes that a fair stochastic rounding is pinned here on the mathematics, with
+# sr_rand16 as a black box: (1) the word's bits split into two disjoint 16-bit sets, positions
+# 0 / 1 reading one and 2 / 3 the other (so the two halves of a group are independent); (2)
+# over every setting of its 16 bits each position draws every 16-bit value exactly once
+# (uniform R, hence the unbiased rounding probability floor(frac * 2**16) / 2**16); (3) the two
+# positions that read the same bits round up nearly independently; (4) a stochastically rounded
+# dot product has the variance of independent rounding.
+
+
+def _rand16_dependencies():
+    """For each group position, the set of word bits whose flip changes its R (black-box probe)."""
+    base = rng.integers(0, 1 << 32, size=64, dtype=np.uint64).astype(np.uint32)
+    deps = [set() for _ in range(4)]
+    for pos in range(4):
+        r0 = Q.sr_rand16(base, np.full(base.size, pos))
+        for b in range(32):
+            r1 = Q.sr_rand16(base ^ np.uint32(1 << b), np.full(base.size, pos))
+            if np.any(r1 != r0):
+                deps[pos].add(b)
+    return deps
+
+
+def test_sr_group_word_splits_into_two_disjoint_halves():
+    deps = _rand16_dependencies()
+    assert deps[0] == deps[1] and deps[2] == deps[3]
+    assert len(deps[0]) == 16 and len(deps[2]) == 16
+    assert deps[0].isdisjoint(deps[2]) and deps[0] | deps[2] == set(range(32))
+
+
+def _words_over_bits(bits, fixed):
+    """All 2**16 words that take every setting of ``bits`` (16 positions) with the rest from ``fixed``."""
+    bits = sorted(bits)
+    v = np.arange(1 << 16, dtype=np.uint64)
+    w = np.full(v.size, fixed, dtype=np.uint64)
+    for i, b in enumerate(bits):
+        w &= ~np.uint64(1 << b)
+        w |= ((v >> np.uint64(i)) & np.uint64(1)) << np.uint64(b)
+    return w.astype(np.uint32)
+
+
+def test_sr_each_position_draws_every_16_bit_value_once():
+    # exhaustive over the 16 bits a half reads (the other half fixed at several random values):
+    # positions reading those bits see each R in [0, 2**16) exactly once, the others do not move
+    deps = _rand16_dependencies()
+    for fixed in rng.integers(0, 1 << 32, size=3, dtype=np.uint64):
+        for half, (mine, other) in enumerate(((0, 2), (2, 0))):
+            w = _words_over_bits(deps[mine], int(fixed))
+            for pos in (mine, mine + 1):
+                r = Q.sr_rand16(w, np.full(w.size, pos))
+                np.testing.assert_array_equal(np.sort(r), np.arange(1 << 16, dtype=np.uint32))
+            for pos in (other, other + 1):
+                r = Q.sr_rand16(w, np.full(w.size, pos))
+                assert np.all(r == r[0])
+
+
+def _up(r16, frac):
+    """Round-up event of the rule at fraction ``frac`` for random values r16."""
+    return (r16.astype(np.float64) + np.floor(frac * 65536.0)) >= 65536.0
+
+
+@pytest.mark.parametrize("half", [0, 2])
+def test_sr_positions_sharing_bits_round_up_nearly_independently(half):
+    # exact over all 2**16 settings of the shared bits: |corr(up_a, up_b)| <= 1e-3 for every
+    # pair of fractions 0.1 .. 0.9 (measured worst 5.7e-4; dyadic fractions give exactly 0)
+    deps = _rand16_dependencies()
+    w = _words_over_bits(deps[half], 0x5A5A5A5A)
+    ra = Q.sr_rand16(w, np.full(w.size, half))
+    rb = Q.sr_rand16(w, np.full(w.size, half + 1))
+    fracs = [i / 10 for i in range(1, 10)]
+    for fa in fracs:
+        for fb in fracs:
+            ua, ub = _up(ra, fa), _up(rb, fb)
+            pa, pb, pab = ua.mean(), ub.mean(), (ua & ub).mean()
+            corr = (pab - pa * pb) / np.sqrt(pa * (1 - pa) * pb * (1 - pb))
+            assert abs(corr) <= 1e-3, (fa, fb, corr)
+    for f in (0.25, 0.5, 0.75):           # dyadic fractions: exactly independent
+        ua, ub = _up(ra, f), _up(rb, f)
+        assert (ua & ub).mean() == ua.mean() * ub.mean()
+
+
+def test_sr_dot_product_has_the_variance_of_independent_rounding():
+    # sum over M = 2048 elements whose group positions pair equal values ([a, a, b, b]), so a
+    # correlation between the positions that share bits would show in the variance; T trials
+    # draw fresh words through the counter (offset); bar: 4 standard errors of a variance
+    from oracle.philox import element_words
+    M, T = 2048, 3000
+    ab = rng.uniform(0.05, 5.95, size=M // 2).astype(np.float32)
+    v = np.repeat(ab, 2)
+    lo = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v, side="right") - 1].astype(np.float64)
+    hi = Q.E2M1_GRID[np.searchsorted(Q.E2M1_GRID, v, side="right")].astype(np.float64)
+    frac = (v.astype(np.float64) - lo) / (hi - lo)
+    p = np.floor(frac * 65536.0) / 65536.0
+    var_indep = float(np.sum((hi - lo) ** 2 * p * (1 - p)))
+    mean_exact = float(np.sum(lo + (hi - lo) * p))
+    pos = np.arange(M) & 3
+    sums = np.empty(T)
+    for t in range(T):
+        r16 = Q.sr_rand16(element_words(M, 0, seed=31337, copy_id=0, offset=t), pos)
+        sums[t] = F.decode(Q.e2m1_round_stochastic(v, r16), "e2m1").sum()
+    var = sums.var(ddof=1)
+    assert abs(var / var_indep - 1.0) <= 4.0 * np.sqrt(2.0 / (T - 1)), (var, var_indep)
+    assert abs(sums.mean() - mean_exact) <= 4.0 * np.sqrt(var_indep / T)
+
+
 def test_nvfp4_sr_uses_copy_indexed_words():
     z = rng.standard_normal((32, 64)).astype(np.float32)
     A = Q.amax(z)

@@ -47,6 +47,27 @@ def test_margin_halves_and_zero_keeps():
     assert st2.scale == 28672.0
 
 
+def test_nan_amax_holds_the_scale_while_in_the_window():
+    # reading: a NaN amax is not finite, like +Inf -- the maximum over a window holding it is
+    # NaN and the scale is kept; most_recent keeps it for that step only
+    st = Rc.DelayedScalingState("e4m3", 4, Rc.ALGO_MAX)
+    st.update(2.0, 0)
+    assert st.scale == 224.0
+    st.update(np.nan, 1)
+    assert st.scale == 224.0 and np.isnan(st.hist[1])
+    for t in (2, 3, 4):
+        st.update(8.0, t)
+        assert st.scale == 224.0
+    st.update(8.0, 5)                 # slot 1 overwritten: the NaN left the window
+    assert st.scale == 56.0
+    mr = Rc.DelayedScalingState("e4m3", 4, Rc.ALGO_MOST_RECENT)
+    mr.update(2.0, 0)
+    mr.update(np.nan, 1)
+    assert mr.scale == 224.0
+    mr.update(8.0, 2)
+    assert mr.scale == 56.0
+
+
 def test_interval_and_history_len_one():
     st = Rc.DelayedScalingState("e4m3", 8, Rc.ALGO_MAX, interval=2)
     st.update(4.0, 0)

@@ -45,6 +45,28 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(current):
     G.check_no_device_error()
 
 
+def test_noalloc_allocates_no_device_memory():
+    # after a first call (which looks up the array's address), further calls change neither
+    # torch's allocator count nor the device's free memory
+    rows, cols = 4096, 2048
+    dy = gaussian((rows, cols), 1e-3, 77, dtype=torch.bfloat16).to(G.DEV)
+    q_col, dbias, sinv = G.u8(cols, rows), torch.zeros(cols, device=G.DEV), G.scalar()
+    scale = G.scalar(2.0 ** 13)
+
+    def call():
+        te.te_quantize_fp8_dbias_noalloc(dy, te.E5M2, dbias, scale=scale, q_col=q_col, scale_inv_out=sinv)
+
+    call()
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    G.check_no_device_error()
+
+
 def test_noalloc_rejects_more_partial_sums_than_the_scratch_holds():
     dy = torch.zeros(15872, 16384, dtype=torch.bfloat16, device=G.DEV)   # 248 x 16384 partial sums > 2^20
     dbias = torch.zeros(16384, device=G.DEV)
