@@ -43,6 +43,23 @@ class DelayedState:
     def slot(self, i: int):
         return self.scale[i:i + 1], self.scale_inv[i:i + 1], self.amax[i:i + 1]
 
+    FIELDS = ("hist", "scale", "scale_inv", "amax")
+
+    def state_dict(self) -> dict:
+        """Host copy of the recipe state, for a checkpoint (the FP8 metadata a module keeps
+        next to its weights: amax history ring, scale, scale_inv, last amax)."""
+        out = {k: getattr(self, k).detach().to("cpu", copy=True) for k in self.FIELDS}
+        out.update(n=self.n, history_len=self.L)
+        return out
+
+    def load_state_dict(self, sd: dict) -> None:
+        """Restore a checkpoint taken with ``state_dict`` (same tensor count and history length)."""
+        if sd["n"] != self.n or sd["history_len"] != self.L:
+            raise ValueError(f"checkpoint holds {sd['n']} tensors x history {sd['history_len']}, "
+                             f"state has {self.n} x {self.L}")
+        for k in self.FIELDS:
+            getattr(self, k).copy_(sd[k])
+
 
 class QuantLinear:
     """Device buffers of one linear (inputs, outputs, quantized copies) and its GEMM passes."""
@@ -213,6 +230,15 @@ class Layer:
             lin.name = name
         self.step_idx = 0
 
+    def state_dict(self) -> dict:
+        """DelayedScaling state of the layer (both directions) and its step counter, on the host."""
+        return {"fwd": self.fwd.state_dict(), "bwd": self.bwd.state_dict(), "step": self.step_idx}
+
+    def load_state_dict(self, sd: dict) -> None:
+        self.fwd.load_state_dict(sd["fwd"])
+        self.bwd.load_state_dict(sd["bwd"])
+        self.step_idx = int(sd["step"])
+
     def scale_update(self) -> None:
         """DelayedScaling bookkeeping after a step: record amaxes, refresh scales (two launches)."""
         L.te_scale_update(self.recipe, 0, self.fwd.hist, self.fwd.amax, self.fwd.scale, self.fwd.scale_inv,
@@ -329,6 +355,13 @@ class ScheduleStep:
                     self.bufs[key].update(xr=torch.empty(M, K, **u8), xc=torch.empty(K, M, **u8),
                                           wr=torch.empty(N, K, **u8), wc=torch.empty(K, N, **u8),
                                           dr=torch.empty(M, N, **u8), dc=torch.empty(N, M, **u8))
+
+    def state_dict(self) -> dict:
+        return {"fwd": self.fwd.state_dict(), "bwd": self.bwd.state_dict()}
+
+    def load_state_dict(self, sd: dict) -> None:
+        self.fwd.load_state_dict(sd["fwd"])
+        self.bwd.load_state_dict(sd["bwd"])
 
     def run(self, step: int) -> None:
         if self.kind == "bf16":

@@ -117,3 +117,49 @@ def assert_equal_codes(got, exp, what=""):
     bad = np.argwhere(got != exp)
     assert bad.size == 0, f"{what}: {len(bad)} mismatches, first at {bad[:4].tolist()}: " \
                           f"got {[int(got[tuple(b)]) for b in bad[:4]]} exp {[int(exp[tuple(b)]) for b in bad[:4]]}"
+
+
+# ---- GEMM parity bar ---------------------------------------------------------------------------
+
+GEMM_TOL = 1e-3
+
+
+def ulp(x, precision_bits: int) -> np.ndarray:
+    """One unit in the last place of |x| in a binary format with ``precision_bits`` significand
+    bits (24 fp32, 8 bf16), normal range (the exponent is floored at -126)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -126.0)
+    return np.exp2(e - (precision_bits - 1))
+
+
+def check_gemm(got, a64, b64, bias=None, bf16_out=False, what="", tol=GEMM_TOL):
+    """The GEMM parity bar on D = A B^T (+ bias) against the oracle's fp64 product of its own
+    dequantized operands a64 [m, K], b64 [n, K] (``got`` [m, n], the device's outputs widened):
+
+    * relative Frobenius error <= tol: fp32 outputs against the fp64 product, bf16 outputs
+      against the bf16-rounded fp64 product (bf16 rounding alone is ~1.7e-3 on Gaussian data);
+    * every element within K * 2^-23 * sum_k |a_k b_k| (fp32 accumulation over K terms) plus
+      one output ulp of the product (the epilogue's rounding), so that a few wrong elements
+      cannot hide under the norm.
+    Returns (rel-Frobenius, largest |error| / bound)."""
+    from oracle import formats as F
+    from oracle import gemm as OG
+    a64 = np.asarray(a64, np.float64)
+    b64 = np.asarray(b64, np.float64)
+    got = np.asarray(got, np.float64)
+    ref = OG.gemm(a64, b64, bias=bias)
+    assert np.isfinite(got).all(), f"{what}: non-finite outputs"
+    exp = F.bf16_bits_to_f32(F.f64_to_bf16_bits(ref)).astype(np.float64) if bf16_out else ref
+    err = OG.rel_frobenius(got, exp)
+    K = a64.shape[1]
+    S = np.abs(a64) @ np.abs(b64).T
+    bound = K * 2.0 ** -23 * S + ulp(ref, 8 if bf16_out else 24)
+    ratio = np.abs(got - ref) / bound
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert err <= tol, f"{what}: rel-Frobenius {err:.3e}"
+    if worst > 1.0:
+        i = np.unravel_index(int(np.argmax(ratio)), ratio.shape)
+        raise AssertionError(f"{what}: element {i} off by {abs(got[i] - ref[i]):.3e} > bound {bound[i]:.3e} "
+                             f"({int(np.sum(ratio > 1))} elements out of bound)")
+    return err, worst

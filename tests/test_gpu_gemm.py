@@ -23,18 +23,11 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-3
 
 
-def _cmp(D, ref, what):
-    ref = np.asarray(ref, np.float64)
-    if D.dtype == torch.bfloat16:
-        got = G.f32_np(D).astype(np.float64)
-        exp = F.bf16_bits_to_f32(F.f64_to_bf16_bits(ref)).astype(np.float64)
-    else:
-        got = D.detach().cpu().numpy().astype(np.float64)
-        exp = ref
-    err = OG.rel_frobenius(got, exp)
-    assert np.isfinite(got).all(), what
-    assert err <= TOL, f"{what}: rel-Frobenius {err:.3e}"
-    return err
+def _cmp(D, A64, B64, bias, what):
+    """Parity of a whole output D against the oracle: rel-Frobenius and element-wise bar."""
+    bf16 = D.dtype == torch.bfloat16
+    got = G.f32_np(D) if bf16 else D.detach().cpu().numpy()
+    return G.check_gemm(got, A64, B64, bias=bias, bf16_out=bf16, what=what)
 
 
 def _linear(M, Kin, Nout, seed):
@@ -64,8 +57,7 @@ def test_bf16_three_passes(M, Kin, Nout, out):
         D = torch.empty(*dshape, dtype=out, device=G.DEV)
         te.te_gemm_bf16(A, B, D, bias, a_layout=la, b_layout=lb)
         torch.cuda.synchronize()
-        ref = OG.gemm(A32, B32, bias=None if bias is None else b.cpu().numpy())
-        _cmp(D, ref, f"bf16 {name}")
+        _cmp(D, A32, B32, None if bias is None else b.cpu().numpy(), f"bf16 {name}")
     G.check_no_device_error()
 
 
@@ -104,7 +96,7 @@ def test_fp8_three_passes(M, Kin, Nout, out):
         D = torch.empty(A.shape[0], B.shape[0], dtype=out, device=G.DEV)
         te.te_gemm_fp8(A, fa, B, fb, sa, sb, D, bias)
         torch.cuda.synchronize()
-        _cmp(D, OG.gemm(A64, B64, bias=None if bias is None else b.cpu().numpy()), f"fp8 {name}")
+        _cmp(D, A64, B64, None if bias is None else b.cpu().numpy(), f"fp8 {name}")
     G.check_no_device_error()
 
 
@@ -163,7 +155,7 @@ def test_mxfp8_three_passes(M, Kin, Nout, out):
         D = torch.empty(A.shape[0], B.shape[0], dtype=out, device=G.DEV)
         te.te_gemm_mxfp8(A, sA, B, sB, D, bias)
         torch.cuda.synchronize()
-        _cmp(D, OG.gemm(A64, B64, bias=None if bias is None else b.cpu().numpy()), f"mxfp8 {name}")
+        _cmp(D, A64, B64, None if bias is None else b.cpu().numpy(), f"mxfp8 {name}")
     G.check_no_device_error()
 
 
@@ -221,7 +213,7 @@ def test_nvfp4_three_passes(M, Kin, Nout, out):
         D = torch.empty(A.shape[0], B.shape[0], dtype=out, device=G.DEV)
         te.te_gemm_nvfp4(A, sA, gA, B, sB, gB, D, bias)
         torch.cuda.synchronize()
-        _cmp(D, OG.gemm(A64, B64, bias=None if bias is None else b.cpu().numpy()), f"nvfp4 {name}")
+        _cmp(D, A64, B64, None if bias is None else b.cpu().numpy(), f"nvfp4 {name}")
     G.check_no_device_error()
 
 
@@ -269,8 +261,7 @@ def test_codonfm_attn_out_fprop_sampled(kind):
         B64 = np.stack([wq_o[idx[int(c - c % 16)] * 16 + c % 16] for c in cols])
     torch.cuda.synchronize()
     got = D.cpu().numpy()[np.ix_(rows, cols)]
-    err = OG.rel_frobenius(got, OG.gemm(A64, B64))
-    assert err <= TOL, f"{kind}: {err:.3e}"
+    G.check_gemm(got, A64, B64, what=kind)
     G.check_no_device_error()
 
 
@@ -296,11 +287,8 @@ def test_codonfm_mlp_down_fprop_sampled(kind):
         A64 = Q.fp8_dequant(Q.fp8_cast(x32[rows], sx, "e4m3"), six, "e4m3")
         B64 = Q.fp8_dequant(Q.fp8_cast(w32[cols], sw, "e4m3"), siw, "e4m3")
     torch.cuda.synchronize()
-    got = G.f32_np(D)[np.ix_(rows, cols)].astype(np.float64)
-    ref = OG.gemm(A64, B64, bias=b.cpu().numpy()[cols])
-    exp = F.bf16_bits_to_f32(F.f64_to_bf16_bits(ref)).astype(np.float64)
-    err = OG.rel_frobenius(got, exp)
-    assert err <= TOL, f"{kind}: {err:.3e}"
+    got = G.f32_np(D)[np.ix_(rows, cols)]
+    G.check_gemm(got, A64, B64, bias=b.cpu().numpy()[cols], bf16_out=True, what=kind)
     G.check_no_device_error()
 
 
@@ -337,8 +325,7 @@ def test_codonfm_wgrad_sampled(kind):
             Q.rht16(np.ascontiguousarray(x32[:, c:c + 1].T), SIGNS), Ax)) for c in cols])
     torch.cuda.synchronize()
     got = D.cpu().numpy()[np.ix_(rows, cols)]
-    err = OG.rel_frobenius(got, OG.gemm(A64, B64))
-    assert err <= TOL, f"{kind}: {err:.3e}"
+    G.check_gemm(got, A64, B64, what=kind)
     G.check_no_device_error()
 
 
