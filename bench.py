@@ -499,7 +499,7 @@ def run_case(args):
     for _ in range(max(warm, 1)):
         fn()
     torch.cuda.synchronize()
-    flush = None if args.no_flush or args.iters == 1 else torch.zeros(68 << 20, dtype=torch.float32, device=dev)
+    flush = None if args.no_flush else torch.zeros(68 << 20, dtype=torch.float32, device=dev)
     if flush is not None:
         flush.sum()
         torch.cuda.synchronize()

@@ -97,7 +97,7 @@ struct Cfg {
   static constexpr int kSmemStage = kSmemSfb + kStages * kSfbBytes;      // epilogue staging, 2 KB per warp
   static constexpr int kSmemBar = kSmemStage + kEpiWarps * 2048;
   static constexpr int kSmemTotal = kSmemBar + 256 + 1024;  // barriers + alignment slack
-  static_assert((3 * kStages + 7) * 8 + 8 <= 256, "barrier area");
+  static_assert((4 * kStages + 7) * 8 + 8 <= 256, "barrier area");
   static_assert(!kBlockScaled || kSfTmemBase + kStages * (kSfaCols + kSfbCols) <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemTotal <= 232448, "shared memory budget");
 };
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint64_t* sf_ready = drain + 1;  // [kStages]: the stage's scale factors are in TMEM
   uint64_t* epi_done = sf_ready + kStages;  // [2]: this CTA's epilogue warps have drained the accumulator
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done + 2);
+  uint64_t* sf_full = epi_done + 2;         // [kStages]: the stage's scale atoms have landed (block-scaled kinds)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -176,7 +177,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       dev::mbar_init(&epi_done[s], kEpiWarps);
     }
     dev::mbar_init(drain, 1);
-    for (int st = 0; st < kStages; ++st) dev::mbar_init(&sf_ready[st], C::kSfCopiers);
+    for (int st = 0; st < kStages; ++st) {
+      dev::mbar_init(&sf_ready[st], C::kSfCopiers);
+      dev::mbar_init(&sf_full[st], 1);
+    }
     *abort_flag = 0;
     dev::fence_barrier_init();
     dev::prefetch_tmap(&tmA);
@@ -229,9 +233,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       uint32_t issued_phase[kStages];
       bool issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-      // pairs: the leader's full barrier counts both CTAs' bytes
-      const uint32_t tx = kPair ? (C::kABytes + C::kBBytes + C::kSfaBytes + C::kSfbBytes) * CG
-                                : C::kABytes + C::kBBytes + C::kSfaBytes;
+      // pairs: the leader's barriers count both CTAs' bytes.  Block-scaled kinds: the scale
+      // atoms are loaded first and land on their own barrier (sf_full), so the copier warps
+      // move them into TMEM while the stage's operand tiles are still arriving.
+      const uint32_t tx = kPair ? (C::kABytes + C::kBBytes) * CG : C::kABytes + C::kBBytes;
+      const uint32_t sf_tx0 = kPair ? (C::kSfaBytes + C::kSfbBytes) * CG : C::kSfaBytes;
       bool ok = !*abort_flag;
       for (int tile = unit; tile < num_tiles && ok; tile += units) {
         int mt, nt;
@@ -241,21 +247,47 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
             ok = false;
             break;
           }
-          uint32_t bytes = tx;
-          int sfb_halves = 0;
+          uint32_t sf_tx = sf_tx0;
           if (C::kBlockScaled && !kPair) {
             for (int h = 0; h < 2; ++h)
-              if (nt * 2 + h < args.sfb_row_atoms) ++sfb_halves;
-            bytes += sfb_halves * C::kSfAtoms * 512;
+              if (nt * 2 + h < args.sfb_row_atoms) sf_tx += C::kSfAtoms * 512;
           }
-          if (leader) dev::mbar_expect_tx(&full[stage], bytes);
+          if (leader) {
+            if (C::kBlockScaled) dev::mbar_expect_tx(&sf_full[stage], sf_tx);
+            dev::mbar_expect_tx(&full[stage], tx);
+          }
           const int arow = (mt * CG + static_cast<int>(rank)) * BM;         // this CTA's A rows
           const int brow = nt * BN + static_cast<int>(rank) * C::kBRows;    // this CTA's B rows
           const uint32_t full_c = dev::mapa_shared(dev::smem_u32(&full[stage]), 0);
+          const uint32_t sf_full_c = dev::mapa_shared(dev::smem_u32(&sf_full[stage]), 0);
           auto load = [&](uint8_t* dst, const CUtensorMap* map, int x, int y) {
             if (kPair) dev::tma_load_2d_pair(dst, map, full_c, x, y);
             else dev::tma_load_2d(dst, map, &full[stage], x, y);
           };
+          auto load_sf = [&](uint8_t* dst, const CUtensorMap* map, int x, int y) {
+            if (kPair) dev::tma_load_2d_pair(dst, map, sf_full_c, x, y);
+          };
+          if (C::kBlockScaled && kPair) {
+            // scale atoms by TMA, first (completion on the leader's sf_full barrier): the scale
+            // tensor is viewed as 256-byte rows, so a 128-row group's atoms of one k-tile are
+            // 2 * kSfAtoms consecutive rows; boxes past the end are zero-filled
+            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
+            load_sf(sSfa + stage * C::kSfaBytes, &tmSa, 0,
+                    static_cast<int>(((mt * CG + static_cast<int>(rank)) * args.sf_katoms + katom) * 2));
+            for (int h = 0; h < 2; ++h)
+              load_sf(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512, &tmSb, 0,
+                      static_cast<int>(((nt * 2 + h) * args.sf_katoms + katom) * 2));
+          } else if (C::kBlockScaled) {
+            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
+            dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
+                           C::kSfaBytes, &sf_full[stage]);
+            for (int h = 0; h < 2; ++h) {
+              const int ra = nt * 2 + h;
+              if (ra < args.sfb_row_atoms)
+                dev::bulk_load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512,
+                               args.sfb + (ra * args.sf_katoms + katom) * 512, C::kSfAtoms * 512, &sf_full[stage]);
+            }
+          }
           if (KIND == kBF16 && args.a_mn) {
             // [K, M] storage: 64 K-rows x 64 M-elements (128 B) per box, two boxes along M
 #pragma unroll
@@ -270,27 +302,6 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
           } else {
             load(sB + stage * C::kBBytes, &tmB, kt * 128, brow);
           }
-          if (C::kBlockScaled && kPair) {
-            // scale atoms by TMA (completion on the leader's barrier): the scale tensor is
-            // viewed as 256-byte rows, so a 128-row group's atoms of one k-tile are
-            // 2 * kSfAtoms consecutive rows; boxes past the end are zero-filled
-            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
-            load(sSfa + stage * C::kSfaBytes, &tmSa, 0,
-                 static_cast<int>(((mt * CG + static_cast<int>(rank)) * args.sf_katoms + katom) * 2));
-            for (int h = 0; h < 2; ++h)
-              load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512, &tmSb, 0,
-                   static_cast<int>(((nt * 2 + h) * args.sf_katoms + katom) * 2));
-          } else if (C::kBlockScaled) {
-            const int64_t katom = static_cast<int64_t>(kt) * C::kSfAtoms;
-            dev::bulk_load(sSfa + stage * C::kSfaBytes, args.sfa + (mt * args.sf_katoms + katom) * 512,
-                           C::kSfaBytes, &full[stage]);
-            for (int h = 0; h < 2; ++h) {
-              const int ra = nt * 2 + h;
-              if (ra < args.sfb_row_atoms)
-                dev::bulk_load(sSfb + stage * C::kSfbBytes + h * C::kSfAtoms * 512,
-                               args.sfb + (ra * args.sf_katoms + katom) * 512, C::kSfAtoms * 512, &full[stage]);
-            }
-          }
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == kStages) stage = 0, phase ^= 1u;
@@ -302,7 +313,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
         // leader, whose exit waits on the final cluster barrier).
         volatile int dummy = 0;
         for (int s = 0; s < kStages; ++s)
-          if (issued[s]) dev::mbar_wait(&full[s], issued_phase[s], &dummy, args.err);
+          if (issued[s]) {
+            dev::mbar_wait(&full[s], issued_phase[s], &dummy, args.err);
+            if (C::kBlockScaled) dev::mbar_wait(&sf_full[s], issued_phase[s], &dummy, args.err);
+          }
       }
     }
   } else if (warp == 1) {
@@ -399,9 +413,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       uint32_t last_phase = 0;
       for (int tile = unit; tile < num_tiles && ok; tile += units) {
         for (int kt = 0; kt < args.k_tiles; ++kt) {
-          // full[stage] of this phase also means the MMAs that read the slot's previous
+          // sf_full[stage] of this phase also means the MMAs that read the slot's previous
           // contents have completed (the producer refilled the stage only after they did)
-          if (!dev::mbar_wait<kPair>(&full[stage], phase, abort_flag, args.err)) {
+          if (!dev::mbar_wait<kPair>(&sf_full[stage], phase, abort_flag, args.err)) {
             ok = false;
             break;
           }
