@@ -955,6 +955,15 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
     // through the sign flip, the Hadamard butterflies, the 1/4 and the block scaling.
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
+      // The block's random words depend only on its position: drawn first, so that the
+      // generator's dependent rounds overlap the loads and the butterflies below.
+      uint4 rnd_a = make_uint4(0, 0, 0, 0), rnd_b = rnd_a;
+      if (SR) {
+        const uint64_t g = static_cast<uint64_t>(c0 + 2 * lane) * static_cast<uint64_t>(a.R) +
+                           static_cast<uint64_t>(r0 + b * 16);
+        rnd_a = nv_rand(a, g, 1u);
+        rnd_b = nv_rand(a, g + static_cast<uint64_t>(a.R), 1u);
+      }
       float2 y[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
@@ -967,12 +976,15 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
 #pragma unroll
         for (int r = 0; r < 16; ++r) y[r] = __fmul2_rn(y[r], make_float2(0.25f, 0.25f));
       }
-      float ma = 0.0f, mb = 0.0f;
+      // block maxima as a tree (the maximum is exact in any order)
+      float ta[16], tb[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        ma = fmaxf(ma, fabsf(y[r].x));
-        mb = fmaxf(mb, fabsf(y[r].y));
-      }
+      for (int r = 0; r < 16; ++r) ta[r] = fabsf(y[r].x), tb[r] = fabsf(y[r].y);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int r = 0; r < w; ++r) ta[r] = fmaxf(ta[r], ta[r + w]), tb[r] = fmaxf(tb[r], tb[r + w]);
+      float ma = ta[0], mb = tb[0];
       if (two_d) ma = mb = lanes_max<8>(fmaxf(ma, mb));  // 16 rows x 16 columns
       const uint32_t sa = nv_scale_code(ma, senc), sb = nv_scale_code(mb, senc);
       codes[0] |= sa << (8 * b);
@@ -984,13 +996,6 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
         const float2 t = __fmul2_rn(y[r], rr);
         va[r] = t.x;
         vb[r] = t.y;
-      }
-      uint4 rnd_a = make_uint4(0, 0, 0, 0), rnd_b = rnd_a;
-      if (SR) {
-        const uint64_t g = static_cast<uint64_t>(c0 + 2 * lane) * static_cast<uint64_t>(a.R) +
-                           static_cast<uint64_t>(r0 + b * 16);
-        rnd_a = nv_rand(a, g, 1u);
-        rnd_b = nv_rand(a, g + static_cast<uint64_t>(a.R), 1u);
       }
       const uint2 qa = nv_encode16<SR>(va, rnd_a), qb = nv_encode16<SR>(vb, rnd_b);
       // two 16-row blocks share one 16-byte chunk of the 32-byte box row
