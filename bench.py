@@ -806,6 +806,7 @@ def run_e2e(layer, args, ws):
     h2d = sum(t.numel() * t.element_size() for tup in host_in for t in tup)
     d2h = sum(t.numel() * t.element_size() for tup in host_out for t in tup)
     hs = HostStreamedLayer(layer, host_in, host_out)
+    link = host_link(host_in, host_out, lins)
     for _ in range(2):
         hs.step(HEADLINE[0])
     torch.cuda.synchronize()
@@ -822,9 +823,56 @@ def run_e2e(layer, args, ws):
     e1.record(main_s)
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), ws) / args.e2e_steps      # per replica (max over ranks)
+    link["bound_ms_per_layer"] = round(1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                                                 (h2d + d2h) / (link["both_gbs"] * 1e9)), 3)
     return {"value": round(ms, 4), "unit": "ms/layer", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "recipe": HEADLINE[0], "steps": args.e2e_steps,
-            "overlap": "per-linear input / output copies on their own streams overlap the compute"}
+            "overlap": "per-linear input / output copies on their own streams overlap the compute",
+            "host_link": link}
+
+
+def host_link(host_in, host_out, lins):
+    """This box's pinned host <-> device bandwidth, measured before the end-to-end run: the largest
+    input copied in, the largest output copied out, then both at once on two streams (the
+    end-to-end figure cannot beat the layer's bytes at these rates)."""
+    import torch
+    src = max((t for tup in host_in for t in tup), key=lambda t: t.numel() * t.element_size())
+    out_dev = max((t for l in lins for t in (l.y, l.dx, l.dw)), key=lambda t: t.numel() * t.element_size())
+    dst_dev = torch.empty_like(src, device=out_dev.device)
+    dst_host = torch.empty_like(out_dev, device="cpu").pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=3):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        return best
+
+    bi, bo = src.numel() * src.element_size(), out_dev.numel() * out_dev.element_size()
+    t_in = timed(lambda: dst_dev.copy_(src, non_blocking=True))
+    t_out = timed(lambda: dst_host.copy_(out_dev, non_blocking=True))
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            dst_dev.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s2):
+            dst_host.copy_(out_dev, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+    t_both = timed(both)
+    del dst_dev, dst_host
+    return {"h2d_gbs": round(bi / t_in / 1e9, 1), "d2h_gbs": round(bo / t_out / 1e9, 1),
+            "both_gbs": round((bi + bo) / t_both / 1e9, 1)}
 
 
 if __name__ == "__main__":
