@@ -42,7 +42,8 @@
 // region and rely on the early release of the register drain for overlap.
 // Tiles are visited in a grouped raster (16 pair M-tiles, 4096 rows, per group) so
 // concurrently running CTAs share A and B tiles in L2, and B is streamed from DRAM
-// once per group.  No cluster multicast is used.
+// once per group; each CTA walks K forwards on its even tiles and backwards on its odd
+// ones, so that consecutive waves of tiles meet in L2.  No cluster multicast is used.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -237,10 +238,16 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       const uint32_t tx = kPair ? (C::kABytes + C::kBBytes) * CG : C::kABytes + C::kBBytes;
       const uint32_t sf_tx0 = kPair ? (C::kSfaBytes + C::kSfbBytes) * CG : C::kSfaBytes;
       bool ok = !*abort_flag;
-      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+      int it = 0;
+      for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         int mt, nt;
         tile_coords(tile, args.m_tiles, args.n_tiles, mt, nt);
-        for (int kt = 0; kt < args.k_tiles; ++kt) {
+        for (int kt0 = 0; kt0 < args.k_tiles; ++kt0) {
+          // Every other tile of a CTA walks K backwards: the CTAs run their tiles in waves,
+          // and a wave that starts where the previous one ended finds the panels' last
+          // k-slices still in L2 (FP8, 12 layer shapes: DRAM traffic 2.16 -> 1.72 x the
+          // operands, 1-2 % faster).  Only the order of the fp32 partial sums changes.
+          const int kt = (it & 1) ? args.k_tiles - 1 - kt0 : kt0;
           if (!dev::mbar_wait<kPair>(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
             ok = false;
             break;
