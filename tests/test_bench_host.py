@@ -73,3 +73,60 @@ def test_reference_arm_prints_contract_line():
     assert line["impl"] == "reference" and line["unit"] == "ms/layer" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _bench():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_per_gemm_table_rates_and_fractions():
+    bench = _bench()
+    pk = {"bf16_tflops_sustained": 1000.0}
+    M, N, K = 1024, 2048, 4096
+    per_g = {("fp8_current", "autocast", "qkv", "fprop", M, N, K): [1.0, 3.0],     # mean 2 ms
+             ("nvfp4", "prequant", "mlp_up", "wgrad", M, N, K): [0.5]}
+    t = bench.per_gemm_table(per_g, pk)
+    assert t["fields"] == bench.PER_GEMM_FIELDS
+    rows = {(r[0], r[3]): r for r in t["rows"]}
+    fl = 2.0 * M * N * K
+    r = rows[("fp8_current", "fprop")]
+    assert r[7] == 2.0 and r[8] == round(fl / 2e-3 / 1e12, 1)
+    assert r[9] == round(fl / 2e-3 / 1e12 / 2000.0, 4)          # FP8: 2 x the bf16 peak
+    r = rows[("nvfp4", "wgrad")]
+    assert r[9] == round(fl / 0.5e-3 / 1e12 / 6000.0, 4)        # NVFP4: 6 x the bf16 peak
+
+
+def test_nvfp4_over_bf16_ratios():
+    bench = _bench()
+    per = {"bf16/autocast": {"ms_per_layer": 12.0, "gemm_ms_per_layer": 11.0},
+           "nvfp4/autocast": {"ms_per_layer": 6.0, "gemm_ms_per_layer": 4.0},
+           "nvfp4/prequant": {"ms_per_layer": 4.0, "gemm_ms_per_layer": 3.5}}
+    r = bench.nvfp4_over_bf16(per)
+    assert r["autocast"] == 2.0 and r["prequant_kernel_only"] == round(11.0 / 3.5, 3)
+    assert bench.nvfp4_over_bf16({"bf16/autocast": per["bf16/autocast"]}) is None
+
+
+def test_fp8_gemm_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The committed DRAM figures are reported only for the GEMM source they were measured on."""
+    bench = _bench()
+    prof = os.path.join(ROOT, "profiles", "gemm_fp8_dram_traffic_codonfm_layer.json")
+    d = json.load(open(prof))
+    assert d["traffic_bytes_per_launch"] > d["algorithmic_bytes_per_launch"] > 0
+    assert len(d["per_shape"]) == 12
+    mean = sum(p["dram_read"] + p["dram_write"] for p in d["per_shape"]) // 12
+    assert abs(mean - d["traffic_bytes_per_launch"]) <= 1
+    # a copy of the tree: unchanged sources give the figure, an edited kernel gives none
+    csrc = tmp_path / "nvfp4_precision_transformer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "gemm_fp8_dram_traffic_codonfm_layer.json").write_text(open(prof).read())
+    for name in ("gemm.cu", "common.cuh"):
+        (csrc / name).write_bytes(open(os.path.join(ROOT, "nvfp4_precision_transformer_gb300", "csrc", name), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    traffic, alg, note = bench.fp8_gemm_traffic()
+    assert (traffic, alg) == (d["traffic_bytes_per_launch"], d["algorithmic_bytes_per_launch"]), note
+    (csrc / "gemm.cu").write_bytes((csrc / "gemm.cu").read_bytes() + b"\n// edited\n")
+    traffic, alg, note = bench.fp8_gemm_traffic()
+    assert traffic is None and alg == d["algorithmic_bytes_per_launch"] and "changed" in note
