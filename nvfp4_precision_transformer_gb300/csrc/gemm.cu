@@ -653,7 +653,14 @@ te_status launch_gemm(const void* A, const void* B, int64_t row_bytes, const uin
   g.b_mn = b_mn;
   g.err = err;
   const int tiles = g.m_tiles * g.n_tiles;
-  const int units = tiles < max_clusters[dev_id] ? tiles : max_clusters[dev_id];
+  // The fewest CTA pairs that keep the number of waves: every pair runs the same number of
+  // tiles (within one), and the SMs left idle leave their share of the power budget to the
+  // busy ones (FP8 / MXFP8 layer GEMMs 1.4-1.7 % faster than with one pair per two SMs).
+  int units = tiles < max_clusters[dev_id] ? tiles : max_clusters[dev_id];
+  if (units > 0) {
+    const int waves = (tiles + units - 1) / units;
+    units = (tiles + waves - 1) / waves;
+  }
   cfg.gridDim = dim3(static_cast<unsigned>(CG * units), 1, 1);
   if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, ta, tb, td, tsa, tsb, g) != cudaSuccess)
     return record_cuda(cudaGetLastError());
