@@ -17,7 +17,8 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("rows,cols,dtype", [(15872 // 8, 4096, torch.bfloat16), (208, 336, torch.bfloat16),
+@pytest.mark.parametrize("rows,cols,dtype", [(15872, 4096, torch.bfloat16), (15872 // 8, 4096, torch.bfloat16),
+                                             (208, 336, torch.bfloat16),
                                              (64, 64, torch.float32), (96, 48, torch.float32), (16, 16, torch.bfloat16)])
 @pytest.mark.parametrize("current", [0, 1])
 def test_fp8_dbias_fused(rows, cols, dtype, current):

@@ -60,3 +60,34 @@ def test_layernorm_rejects_and_optional_outputs():
     with pytest.raises(te.TEError):
         te.te_layernorm_fp8(x, g, b, -1.0, te.E4M3, G.scalar(1.0), q)             # eps must be >= 0
     G.check_no_device_error()
+
+
+@pytest.mark.parametrize("rows,cols", [(15872, 4096), (15872, 2048), (2048, 8192)])
+def test_layernorm_fp8_many_rows_per_group(rows, cols):
+    """Enough rows that every row group (register kernel) or warp (shared-memory kernel, 8192
+    columns) walks several rows, so the row loop's reuse of its buffers and barriers is exercised:
+    sampled rows against the oracle, every FP8 code against the oracle's cast of the kernel's own
+    bf16 output, the amax over all of it."""
+    x = student_t_outliers((rows, cols), 77 + cols, dtype=torch.bfloat16).to(G.DEV)
+    gamma = (1.0 + gaussian((cols,), 0.1, 78, dtype=torch.float32)).to(G.DEV)
+    beta = gaussian((cols,), 0.1, 79, dtype=torch.float32).to(G.DEV)
+    eps, scale_v = 1e-5, 2.0 ** 5
+    q = G.u8(rows, cols)
+    ln = torch.empty(rows, cols, dtype=torch.bfloat16, device=G.DEV)
+    mu, rs = torch.empty(rows, device=G.DEV), torch.empty(rows, device=G.DEV)
+    amax = G.scalar(-1.0)
+    te.te_layernorm_fp8(x, gamma, beta, eps, te.E4M3, G.scalar(scale_v), q, ln, mu, rs, amax)
+    torch.cuda.synchronize()
+    G.check_no_device_error()
+    rng = np.random.default_rng(rows + cols)
+    idx = np.unique(np.concatenate([rng.choice(rows, 256, replace=False), [0, 1, rows - 2, rows - 1]]))
+    x32 = G.f32_np(x[torch.from_numpy(idx).to(G.DEV)])
+    y64, mu64, rs64 = layernorm(x32, gamma.cpu().numpy(), beta.cpu().numpy(), eps)
+    np.testing.assert_allclose(mu.cpu().numpy()[idx], mu64, rtol=1e-5, atol=1e-6 * np.abs(x32).max())
+    np.testing.assert_allclose(rs.cpu().numpy()[idx], rs64, rtol=1e-5)
+    ln_s = G.f32_np(ln[torch.from_numpy(idx).to(G.DEV)]).astype(np.float64)
+    ulp = np.maximum(np.abs(y64), 2.0 ** -126) * 2.0 ** -8
+    assert np.all(np.abs(ln_s - y64) <= ulp + 1e-5 * np.abs(y64) + 1e-6)
+    ln32 = G.f32_np(ln)
+    G.assert_equal_codes(q.cpu().numpy(), Q.fp8_cast(ln32, scale_v, "e4m3"), "LN FP8 codes, all rows")
+    assert np.float32(amax.item()) == Q.amax(ln32)
