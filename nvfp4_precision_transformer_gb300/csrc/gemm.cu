@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
   }
   __syncthreads();
 
-  // Scale atoms of stage `st` (shared memory) -> its TMEM slot, one copy per 512-byte atom.
-  auto issue_sf_copies = [&](int st, int jlo, int jhi) {
+  // Scale atoms j = j0, j0 + dj, ... of stage `st` (shared memory) -> its TMEM slot, one copy
+  // per 512-byte atom, the A atom and the two B atoms of a k-step back to back (grouped by
+  // k-step the copies run 15-30 % faster than grouped by operand).
+  auto issue_sf_copies = [&](int st, int j0, int dj) {
     const uint32_t sfa_t = tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
     const uint32_t sfb_t = sfa_t + C::kSfaCols;
     const uint32_t sfa_s = dev::smem_u32(sSfa + st * C::kSfaBytes);
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
     };
 #pragma unroll
     for (int j = 0; j < C::kSfAtoms; ++j) {
-      if (j < jlo || j >= jhi) continue;
+      if (j < j0 || (j - j0) % dj != 0) continue;
       cp(sfa_t + 4 * j, sfa_s + 512 * j);
 #pragma unroll
       for (int h = 0; h < 2; ++h) cp(sfb_t + 8 * j + 4 * h, sfb_s + h * C::kSfAtoms * 512 + 512 * j);
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
-      auto copy_sf = [&](int st) { issue_sf_copies(st, 0, C::kSfAtoms); };
+      auto copy_sf = [&](int st) { issue_sf_copies(st, 0, 1); };
       for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
     // ------------------------------------------------ scale-factor copiers (one thread each; the pair's leader)
     const int copier = warp - kCopyWarp;
     if (C::kSfCopier && lane == 0 && leader) {
-      const int jlo = copier * C::kSfAtoms / C::kSfCopiers, jhi = (copier + 1) * C::kSfAtoms / C::kSfCopiers;
+      // NVFP4: copier c takes the k-steps c, c + 2 (1 % faster than k-steps 2c, 2c + 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = !*abort_flag;
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
             break;
           }
           dev::tc_fence_after();
-          issue_sf_copies(stage, jlo, jhi);
+          issue_sf_copies(stage, copier, C::kSfCopiers);
           if (kPair) dev::tc_commit_pair(&sf_ready[stage], 1);
           else dev::tc_commit(&sf_ready[stage]);
           last = stage;
