@@ -548,6 +548,21 @@ def per_gemm_table(per_g, pk):
             "timing": "CUDA events around each GEMM launch inside the timed steps (quantizers excluded), mean"}
 
 
+def roofline_by_kind(agg, pk):
+    """Tensor roofline of each GEMM kind over its pre-quantized layer GEMMs in the step (BF16: its
+    autocast run, which has no quantizers): achieved TFLOP/s from the per-GEMM CUDA events against
+    the measured sustained bf16 peak times the nominal dtype ratio."""
+    out = {}
+    for (r, m), d in agg.items():
+        if m != ("autocast" if r == "bf16" else "prequant") or d["gemm_ms"] <= 0:
+            continue
+        tf = d["gemm_flops"] / (d["gemm_ms"] * 1e-3) / 1e12
+        peak = pk["bf16_tflops_sustained"] * PEAK_RATIO[RECIPE_DTYPE[r]]
+        out[r] = {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                  "frac": round(tf / peak, 4)}
+    return out
+
+
 def nvfp4_over_bf16(per):
     """The pages' NVFP4-over-BF16 speed-ups: autocast (quantizers included) and kernel-only
     (pre-quantized NVFP4 GEMMs against the BF16 GEMMs)."""
@@ -695,7 +710,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": round(head_ms / PAGES_MS[HEADLINE], 4), "dtype": "fp8",
             "data": "synthetic", "config": workload_config(args), "per_recipe": per, "per_gemm": per_gemm,
-            "nvfp4_over_bf16": ratios, "roofline": roofline, "gpu_launches": int(launches), "clocks": clocks,
+            "nvfp4_over_bf16": ratios, "roofline": roofline, "roofline_by_kind": roofline_by_kind(agg, pk),
+            "gpu_launches": int(launches), "clocks": clocks,
             "aggregate": {"layers_per_s": round(ws * 1e3 / head_ms, 3), "replicas": ws,
                           "note": "value is ms per layer of one replica (max over ranks); replicas run in parallel"}}
 

@@ -136,3 +136,17 @@ def test_fp8_gemm_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     (csrc / "gemm.cu").write_bytes((csrc / "gemm.cu").read_bytes() + b"\n// edited\n")
     traffic, alg, note = bench.fp8_gemm_traffic()
     assert traffic is None and alg == d["algorithmic_bytes_per_launch"] and "changed" in note
+
+
+def test_roofline_by_kind_uses_prequant_runs_and_dtype_peaks():
+    bench = _bench()
+    pk = {"bf16_tflops_sustained": 1000.0}
+    agg = {("bf16", "autocast"): {"gemm_ms": 2.0, "gemm_flops": 2.0e12},
+           ("nvfp4", "prequant"): {"gemm_ms": 1.0, "gemm_flops": 3.0e12},
+           ("nvfp4", "autocast"): {"gemm_ms": 9.0, "gemm_flops": 3.0e12},
+           ("fp8_current", "prequant"): {"gemm_ms": 1.0, "gemm_flops": 1.5e12}}
+    r = bench.roofline_by_kind(agg, pk)
+    assert set(r) == {"bf16", "nvfp4", "fp8_current"}
+    assert r["bf16"]["achieved"] == 1000.0 and r["bf16"]["frac"] == 1.0
+    assert r["nvfp4"]["achieved"] == 3000.0 and r["nvfp4"]["peak"] == 6000.0 and r["nvfp4"]["frac"] == 0.5
+    assert r["fp8_current"]["peak"] == 2000.0 and r["fp8_current"]["frac"] == 0.75
