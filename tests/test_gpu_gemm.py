@@ -391,3 +391,38 @@ def test_accumulate_of_zero_product_keeps_main_grad_bits():
     np.testing.assert_array_equal(D.cpu().numpy().view(np.uint32), d0.view(np.uint32))
     with pytest.raises(te.TEError):
         te.te_gemm_bf16(A, B, torch.empty(M, N, dtype=torch.bfloat16, device=G.DEV), None, accumulate=1)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "mxfp8", "nvfp4"])
+def test_several_tiles_per_pair_ragged_k(kind):
+    """2304 x 4352 outputs are 153 tiles, three per CTA pair, so the pairs' second tiles walk K
+    backwards; K = 1056 leaves the last 128-byte k-tile partly outside the operands (zero-filled
+    by TMA) on every kind.  The whole output against the oracle's fp64 product."""
+    M, N, K = 2304, 4352, 1056
+    x = gaussian((M, K), 1.0, 611).to(G.DEV)
+    w = gaussian((N, K), 0.02, 612).to(G.DEV)
+    b = gaussian((N,), 0.02, 613, dtype=torch.float32).to(G.DEV)
+    x32, w32 = G.f32_np(x), G.f32_np(w)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device=G.DEV)
+    if kind == "bf16":
+        te.te_gemm_bf16(x, w, D, b)
+        A64, B64 = x32, w32
+    elif kind == "fp8":
+        xr, _, xs = _fp8_current(x, "e4m3")
+        wr, _, ws = _fp8_current(w, "e4m3")
+        te.te_gemm_fp8(xr, te.E4M3, wr, te.E4M3, xs, ws, D, b)
+        A64, B64 = _fp8_oracle(x32, "e4m3")[0], _fp8_oracle(w32, "e4m3")[0]
+    elif kind == "mxfp8":
+        xr, xsr, _, _ = _mx(x)
+        wr, wsr, _, _ = _mx(w)
+        te.te_gemm_mxfp8(xr, xsr, wr, wsr, D, b)
+        A64 = Q.mxfp8_dequant(*Q.mxfp8_quantize(x32))
+        B64 = Q.mxfp8_dequant(*Q.mxfp8_quantize(w32))
+    else:
+        xq, wq = _nv(x, 0), _nv(w, W_FLAGS)
+        te.te_gemm_nvfp4(xq[0], xq[1], xq[2], wq[0], wq[1], wq[2], D, b)
+        A64 = Q.nvfp4_dequant(*Q.nvfp4_quantize(x32, Q.amax(x32)))
+        B64 = Q.nvfp4_dequant(*Q.nvfp4_quantize(w32, Q.amax(w32), block2d=True))
+    torch.cuda.synchronize()
+    _cmp(D, A64, B64, b.cpu().numpy(), f"{kind} {M}x{N}x{K}")
+    G.check_no_device_error()
