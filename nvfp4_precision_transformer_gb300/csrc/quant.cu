@@ -824,6 +824,11 @@ template <int FMT, bool SR>
 struct QLaunch {
   static constexpr int NW = FMT == kQNV ? 11 : 8;
   static constexpr int NS = 2;
+  // NVFP4 launches that write one copy leave out the other copy's staging box, which makes room
+  // for a twelfth warp (SR + RHT col copy 9 % faster, RHT col 6 %, SR row 8 %); the FP8 casts
+  // were slower with more warps.
+  static constexpr int kOneCopyWarps = FMT == kQNV ? 12 : NW;
+  static constexpr int kMaxWarps = kOneCopyWarps > NW ? kOneCopyWarps : NW;
 };
 template <typename T, int FMT, bool SR>
 struct QSmem {
@@ -832,6 +837,15 @@ struct QSmem {
   static constexpr int kWarpBytes = Lc::NS * kQTileBytes + G::ROW_BOX + G::COL_BOX;
   static constexpr int kTotal = Lc::NW * kWarpBytes + 2048 /* barriers + r-tables */ + 1024 /* alignment */;
   static_assert(kTotal <= 232448, "shared memory budget");
+  // one copy: the ring and that copy's box only
+  static constexpr int kWarpBytesRow = Lc::NS * kQTileBytes + G::ROW_BOX;
+  static constexpr int kWarpBytesCol = Lc::NS * kQTileBytes + G::COL_BOX;
+  static constexpr int kTotalRow = Lc::kOneCopyWarps * kWarpBytesRow + 2048 + 1024;
+  static constexpr int kTotalCol = Lc::kOneCopyWarps * kWarpBytesCol + 2048 + 1024;
+  static constexpr int kTotalMax = kTotal > kTotalRow ? (kTotal > kTotalCol ? kTotal : kTotalCol)
+                                                      : (kTotalRow > kTotalCol ? kTotalRow : kTotalCol);
+  static_assert(kTotalMax <= 232448, "shared memory budget");
+  static_assert(Lc::kMaxWarps * Lc::NS * 8 <= 256, "barrier area");
   static_assert(G::ROW_BOX % 1024 == 0 && G::COL_BOX % 1024 == 0, "box alignment");
 };
 
@@ -1089,21 +1103,25 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
 }
 
 template <typename T, int FMT, bool SR>
-__global__ void __launch_bounds__(QLaunch<FMT, SR>::NW * 32, 1)
+__global__ void __launch_bounds__(QLaunch<FMT, SR>::kMaxWarps * 32, 1)
     qtile_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_row,
                  const __grid_constant__ CUtensorMap tm_col, const __grid_constant__ TileArgs a) {
   using G = QGeom<T, FMT>;
   constexpr int TC = G::TC;
-  constexpr int kQWarps = QLaunch<FMT, SR>::NW;
-  constexpr int kQStages = QLaunch<FMT, SR>::NS;
-  constexpr int kQWarpBytes = QSmem<T, FMT, SR>::kWarpBytes;
+  using Sm = QSmem<T, FMT, SR>;
+  using Lc = QLaunch<FMT, SR>;
+  // NVFP4 one-copy launches carry more warps, each with the input ring and that copy's box only
+  const bool one_copy = Lc::kOneCopyWarps != Lc::NW && !(a.do_row && a.do_col);
+  const int kQWarps = Lc::kOneCopyWarps != Lc::NW ? static_cast<int>(blockDim.x >> 5) : Lc::NW;
+  constexpr int kQStages = Lc::NS;
+  const int kQWarpBytes = one_copy ? (a.do_row ? Sm::kWarpBytesRow : Sm::kWarpBytesCol) : Sm::kWarpBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + warp * kQWarpBytes;
   uint8_t* box_row = ring + kQStages * kQTileBytes;
-  uint8_t* box_col = box_row + G::ROW_BOX;
+  uint8_t* box_col = box_row + (one_copy && !a.do_row ? 0 : G::ROW_BOX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQWarps * kQWarpBytes) + warp * kQStages;
   float* rtab = reinterpret_cast<float*>(smem + kQWarps * kQWarpBytes + 256);
 
@@ -1270,7 +1288,7 @@ te_status launch_qtile(const void* x, int64_t R, int64_t C, uint8_t* q_row, uint
   cudaGetDevice(&dev_id);
   if (dev_id >= 0 && dev_id < 64 && !attr_set[dev_id]) {
     if (cudaFuncSetAttribute(qtile_kernel<T, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             QSmem<T, FMT, SR>::kTotal) != cudaSuccess)
+                             QSmem<T, FMT, SR>::kTotalMax) != cudaSuccess)
       return record_cuda(cudaGetLastError());
     attr_set[dev_id] = true;
   }
@@ -1293,13 +1311,15 @@ te_status launch_qtile(const void* x, int64_t R, int64_t C, uint8_t* q_row, uint
   a.err = device_error_word();
   if (a.err == nullptr) return record_cuda(cudaErrorInvalidDevice);
   constexpr int TC = G::TC;
-  constexpr int NW = QLaunch<FMT, SR>::NW;
+  using Sm = QSmem<T, FMT, SR>;
+  const bool one_copy = QLaunch<FMT, SR>::kOneCopyWarps != QLaunch<FMT, SR>::NW && (q_row == nullptr || q_col == nullptr);
+  const int NW = one_copy ? QLaunch<FMT, SR>::kOneCopyWarps : QLaunch<FMT, SR>::NW;
+  const int smem_bytes = one_copy ? (q_row ? Sm::kTotalRow : Sm::kTotalCol) : Sm::kTotal;
   const int64_t tiles = ((R + 63) / 64) * ((C + TC - 1) / TC);
   int64_t grid = (tiles + NW - 1) / NW;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), NW * 32, QSmem<T, FMT, SR>::kTotal, st>>>(tin, trow, tcol,
-                                                                                                   a);
+  qtile_kernel<T, FMT, SR><<<static_cast<unsigned>(grid), NW * 32, smem_bytes, st>>>(tin, trow, tcol, a);
   count_launch();
   return launch_status();
 }
