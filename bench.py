@@ -387,7 +387,8 @@ def workload_config(args):
 
 # ---- our arm ---------------------------------------------------------------------------------------
 
-KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_both", "fp8_col_dbias", "mxfp8_both", "nvfp4_rn_row",
+KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_col", "fp8_both", "fp8_col_dbias", "mxfp8_row",
+                "mxfp8_col", "mxfp8_both", "nvfp4_rn_row",
                 "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "layernorm_fp8",
                 "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4",
                 "cublaslt_bf16", "cublaslt_fp8", "cublaslt_mxfp8", "cublaslt_nvfp4")
@@ -478,6 +479,9 @@ def run_case(args):
             "amax_rht_only": (lambda: te.te_amax_reduce(x, None, amax_r, signs), 2 * n),
             "fp8_row": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, None, amax, sinv), 3 * n),
             "fp8_both": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, qr, qc, amax, sinv), 4 * n),
+            "fp8_col": (lambda: te.te_quantize_fp8(x, te.E4M3, scale, 0, None, qc, amax, sinv), 3 * n),
+            "mxfp8_row": (lambda: te.te_quantize_mxfp8(x, qr, smr), 2 * n + n + n // 32),
+            "mxfp8_col": (lambda: te.te_quantize_mxfp8(x, None, None, qc, smc), 2 * n + n + n // 32),
             "mxfp8_both": (lambda: te.te_quantize_mxfp8(x, qr, smr, qc, smc), 2 * n + 2 * (n + n // 32)),
             "nvfp4_rn_row": (lambda: nv(0, True, False), 2 * n + n // 2 + n // 16),
             "nvfp4_rht_col": (lambda: nv(RHT, False, True), 2 * n + n // 2 + n // 16),
