@@ -674,10 +674,10 @@ __device__ __forceinline__ uint32_t nv_scale_code(float bm, float senc) {
 }
 
 // ---- warp-tile quantizers (FP8, MXFP8, NVFP4) ------------------------------------------------------
-// Persistent CTAs of 8 warps; every warp owns a private 2-stage ring of 64-row x
-// 128-byte input tiles (64 x 64 bf16 or 64 x 32 fp32) that its lane 0 fills with TMA
-// (128-byte swizzle), plus one shared-memory staging box per output copy, so warps
-// never wait on each other.  Per tile, lane l quantizes tile rows l and l + 32 for
+// Persistent CTAs of 8 warps (NVFP4: 11, or 12 when one copy is written); every warp owns
+// a private 2-stage ring of 64-row x 128-byte input tiles (64 x 64 bf16 or 64 x 32 fp32)
+// that its lane 0 fills with TMA (128-byte swizzle), plus one shared-memory staging box per
+// output copy written, so warps never wait on each other.  Per tile, lane l quantizes tile rows l and l + 32 for
 // the row copy (16-byte shared loads, distinct swizzled chunks in every 8-lane
 // phase) and its 4-byte column slice of all 64 rows for the col copy (32 distinct
 // banks per row).  The quantized bytes go to swizzled staging boxes and leave with
