@@ -696,9 +696,23 @@ __device__ __forceinline__ float nv_senc(float A) {
   const float s = __fdiv_rn(2688.0f, A);
   return isfinite(s) ? s : 1.0f;
 }
+// fl32(x / 6), correctly rounded, for x >= 0: the product with fl32(1/6) and one correction
+// step from the exact residual (Markstein's FMA division, IBM J. Res. Dev. 34(1), 1990).  An
+// exhaustive check over every float (tests/test_div6_exhaustive.py) finds it equal to the IEEE
+// quotient for all x >= 2^-125; below that the quotient is subnormal and may differ by one
+// ulp, so those inputs take the full division.  (Together with the RHT sign masks hoisted out
+// of the block loop: NVFP4 RHT col copy 5 %, SR + RHT col copy and 2D copies 2 % faster.)
+__device__ __forceinline__ float div6_rn(float x) {
+  if (x >= 0x1p-125f) {
+    const float c = 0x1.555556p-3f;   // fl32(1/6)
+    const float q0 = __fmul_rn(x, c);
+    return __fmaf_rn(__fmaf_rn(-q0, 6.0f, x), c, q0);
+  }
+  return __fdiv_rn(x, 6.0f);
+}
 // UE4M3 block-scale code of a block with amax bm: RN(fl32(fl32(bm / 6) * S_enc)).
 __device__ __forceinline__ uint32_t nv_scale_code(float bm, float senc) {
-  return cvt_e4m3x2(__fmul_rn(__fdiv_rn(bm, 6.0f), senc), 0.0f) & 0x7Fu;
+  return cvt_e4m3x2(__fmul_rn(div6_rn(bm), senc), 0.0f) & 0x7Fu;
 }
 
 // ---- warp-tile quantizers (FP8, MXFP8, NVFP4) ------------------------------------------------------
@@ -996,9 +1010,10 @@ __device__ __forceinline__ void row_pass(const uint8_t* tile, uint8_t* box, int6
 
 // Col copy of one tile: lane handles its 4-byte column slice (NCL columns) of all 64 rows.
 template <typename T, int FMT, bool SR>
+// smask[r]: the RHT sign-flip mask of block row r (zero without RHT), computed once per kernel.
 __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int64_t r0, int64_t c0, const TileArgs& a,
                                          float s_fp8, float senc, const float* rtab, int lane, float& lmax,
-                                         bool track_max) {
+                                         bool track_max, const uint32_t (&smask)[16]) {
   using G = QGeom<T, FMT>;
   constexpr int NCL = G::NCL;
   const bool two_d = FMT == kQNV && (a.flags & TE_NVFP4_2D) != 0;
@@ -1023,7 +1038,7 @@ __device__ __forceinline__ void col_pass(const uint8_t* tile, uint8_t* box, int6
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         uint32_t w = tile_word(tile, b * 16 + r, lane);
-        if (rht) w ^= rht_sign2(a.signs, r);
+        w ^= smask[r];
         y[r] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
       }
       if (rht) {
@@ -1195,6 +1210,11 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::kMaxWarps * 32, 1)
       }
     }
   }
+  // the 16 RHT sign masks of a block's rows, once per kernel instead of once per block
+  uint32_t smask[16];
+  const bool rht_col = FMT == kQNV && (a.flags & TE_NVFP4_RHT_COL) != 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) smask[r] = rht_col ? rht_sign2(a.signs, r) : 0u;
   int abort_flag = 0;
   float lmax = 0.0f;
   int k = 0;
@@ -1207,7 +1227,7 @@ __global__ void __launch_bounds__(QLaunch<FMT, SR>::kMaxWarps * 32, 1)
     if (lane == 0) dev::bulk_wait_read0();  // the previous tile's boxes have been read out
     __syncwarp();
     if (a.do_row) row_pass<T, FMT, SR>(tile, box_row, r0, c0, a, s_fp8, senc_r, rtab, lane, lmax);
-    if (a.do_col) col_pass<T, FMT, SR>(tile, box_col, r0, c0, a, s_fp8, senc_c, rtab + 128, lane, lmax, !a.do_row);
+    if (a.do_col) col_pass<T, FMT, SR>(tile, box_col, r0, c0, a, s_fp8, senc_c, rtab + 128, lane, lmax, !a.do_row, smask);
     if (a.dbias_ws != nullptr) tile_colsum<T>(tile, r0, c0, a, lane);
     dev::fence_proxy_async();  // order this tile's shared-memory reads and box writes before the async copies
     __syncwarp();
