@@ -389,7 +389,8 @@ def workload_config(args):
 
 KERNEL_CASES = ("amax", "amax_rht", "amax_rht_only", "fp8_row", "fp8_col", "fp8_both", "fp8_col_dbias", "mxfp8_row",
                 "mxfp8_col", "mxfp8_both", "nvfp4_rn_row",
-                "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "layernorm_fp8",
+                "nvfp4_rht_col", "nvfp4_sr_row", "nvfp4_sr_rht_col", "nvfp4_2d_both", "nvfp4_2d_row", "nvfp4_2d_col",
+                "layernorm_fp8",
                 "gemm_bf16", "gemm_fp8", "gemm_mxfp8", "gemm_nvfp4",
                 "cublaslt_bf16", "cublaslt_fp8", "cublaslt_mxfp8", "cublaslt_nvfp4")
 
@@ -488,6 +489,9 @@ def run_case(args):
             "nvfp4_sr_row": (lambda: nv(SR, True, False), 2 * n + n // 2 + n // 16),
             "nvfp4_sr_rht_col": (lambda: nv(SR | RHT, False, True), 2 * n + n // 2 + n // 16),
             "nvfp4_2d_both": (lambda: nv(D2, True, True), 2 * n + n + n // 8),
+            # the one-copy 16 x 16 launches autocast runs on W (Fprop row copy, Dgrad col copy)
+            "nvfp4_2d_row": (lambda: nv(D2, True, False), 2 * n + n // 2 + n // 16),
+            "nvfp4_2d_col": (lambda: nv(D2, False, True), 2 * n + n // 2 + n // 16),
         }
         if args.case == "fp8_col_dbias":
             db = torch.empty(C, device=dev)
