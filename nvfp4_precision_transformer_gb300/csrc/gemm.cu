@@ -9,7 +9,7 @@
 // Every kind moves 32 bytes of each operand row per instruction, so one k-tile
 // is a 128-byte row slice (one 128-byte-swizzle atom) and 4 instructions.
 //
-// CTA = 11 warps (NVFP4 12), one CTA per SM (the shared-memory footprint guarantees it):
+// CTA = 10 warps (MXFP8 11, NVFP4 12), one CTA per SM (the shared-memory footprint guarantees it):
 //   warp 0      TMA producer: A tile [128 x 128 B], B tile and, for the block-scaled
 //               kinds, the scale-factor atoms, into a shared-memory ring guarded by
 //               full/empty mbarriers;
@@ -71,13 +71,12 @@ struct Cfg {
   static constexpr int kStages = kPair ? (KIND == kNVFP4 ? 5 : 6) : (KIND == kNVFP4 ? 3 : 4);
   static constexpr bool kBlockScaled = KIND >= kMXFP8;
   static constexpr int kAccStages = kBlockScaled ? 1 : 2;
-  // The scale copies (NVFP4 12, MXFP8 3 per k-tile) go out from a warp of their own,
-  // so the tensor pipe overlaps them with the MMAs (pairs: NVFP4 +12 %, MXFP8 +11 %).
-  static constexpr bool kSfCopier = kBlockScaled;
-  // One thread's copies complete at about one per 46 ns whatever their size, so NVFP4's
-  // 12 per k-tile from one thread outlast the k-tile's MMAs: two copier warps, each
-  // issuing the copies of half the k-steps (+29 %).
-  static constexpr int kSfCopiers = KIND == kNVFP4 ? 2 : 1;
+  // The scale copies (NVFP4 12, MXFP8 3 per k-tile) go out from copier warps of their own,
+  // so the tensor pipe overlaps them with the MMAs (pairs: NVFP4 +12 %, MXFP8 +11 %).  One
+  // thread's copies complete at about one per 46 ns whatever their size, so NVFP4's 12 per
+  // k-tile from one thread outlast the k-tile's MMAs: two copier warps, each issuing the
+  // copies of half the k-steps (+29 %).  BF16 and FP8 have no scales and no copier warp.
+  static constexpr int kSfCopiers = KIND == kNVFP4 ? 2 : (kBlockScaled ? 1 : 0);
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kSfCopiers);
   static constexpr uint32_t kTmemCols = 512u;
   static constexpr int kABytes = BM * 128;
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
     }
     dev::mbar_init(drain, 1);
     for (int st = 0; st < kStages; ++st) {
-      dev::mbar_init(&sf_ready[st], C::kSfCopiers);
+      dev::mbar_init(&sf_ready[st], C::kSfCopiers > 0 ? C::kSfCopiers : 1);
       dev::mbar_init(&sf_full[st], 1);
     }
     *abort_flag = 0;
@@ -352,7 +351,6 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
       auto sf_slot = [&](int st) {
         return tmem_base + C::kSfTmemBase + static_cast<uint32_t>(st * (C::kSfaCols + C::kSfbCols));
       };
-      auto copy_sf = [&](int st) { issue_sf_copies(st, 0, 1); };
       for (int tile = unit; tile < num_tiles && ok; tile += units, ++it) {
         const int as = it % C::kAccStages;
         const uint32_t aphase = static_cast<uint32_t>(it / C::kAccStages) & 1u;
@@ -370,18 +368,17 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
           const uint32_t sfa_t = sf_slot(stage), sfb_t = sfa_t + C::kSfaCols;
           // the stage's addresses first, so that little stands between a barrier's completion
           // and the first MMA (MXFP8 1 % faster); the scale factors of this k-tile reach the
-          // stage's TMEM slot from this thread (in issue order with the MMAs) or from the
-          // copier warps, whose copies run beside this thread's MMAs of earlier k-tiles
+          // stage's TMEM slot from the copier warps, whose copies run beside this thread's
+          // MMAs of earlier k-tiles
           if (!dev::mbar_wait<kPair>(&full[stage], phase, abort_flag, args.err)) {
             ok = false;
             break;
           }
-          if (C::kSfCopier && !dev::mbar_wait<kPair>(&sf_ready[stage], phase, abort_flag, args.err)) {
+          if (C::kBlockScaled && !dev::mbar_wait<kPair>(&sf_ready[stage], phase, abort_flag, args.err)) {
             ok = false;
             break;
           }
           dev::tc_fence_after();
-          if (C::kBlockScaled && !C::kSfCopier) copy_sf(stage);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             // K-major: 128-byte rows, 8-row swizzle atoms 1024 B apart; a k-step advances 32 B.
@@ -424,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::kThreads, 1)
   } else if (warp >= kCopyWarp) {
     // ------------------------------------------------ scale-factor copiers (one thread each; the pair's leader)
     const int copier = warp - kCopyWarp;
-    if (C::kSfCopier && lane == 0 && leader) {
+    if (C::kBlockScaled && lane == 0 && leader) {
       // NVFP4: copier c takes the k-steps c, c + 2 (1 % faster than k-steps 2c, 2c + 1)
       int stage = 0;
       uint32_t phase = 0;
