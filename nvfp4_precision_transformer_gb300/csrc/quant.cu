@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(32 * kLnWarps, 1)
   for (int64_t row = first; row < R; row += stride, ++k) {
     const int bsel = k & 1;
     if (lane == 0 && row + stride < R) fetch(row + stride, bsel ^ 1);   // that buffer's previous row is done
-    // lane 0 waits for the row (bounded) and the warp follows its verdict together
+    // lane 0 waits for the row (bounded) and the warp follows its result together
     int ok = 1;
     if (lane == 0) ok = dev::mbar_wait(&ln_bar[wib][bsel], static_cast<uint32_t>(k >> 1) & 1u, &abort_flag, err);
     __syncwarp();
