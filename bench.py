@@ -817,6 +817,14 @@ def run_schedule(args, cfg, dev, rank, ws):
     return out
 
 
+def e2e_steps(args) -> int:
+    """Steps of the end-to-end run: ``--e2e-steps`` when given, else as many as the device-timed
+    region (at least 5). The copies of consecutive steps overlap as in a training loop, so the
+    pipeline's fill (the first inputs alone on the link) and drain (the last outputs alone) are
+    spread over the same K steps as the bench line's other figures."""
+    return args.e2e_steps if args.e2e_steps > 0 else max(5, args.steps)
+
+
 def run_e2e(layer, args, ws):
     """The headline recipe end to end: every step copies the layer's inputs from pinned host
     memory, runs it, and copies its outputs back (``HostStreamedLayer``: each linear's input
@@ -841,10 +849,7 @@ def run_e2e(layer, args, ws):
     e0.record(main_s)
     for s in hs.streams():
         s.wait_event(e0)
-    # As many steps as the device-timed region: the copies of consecutive steps overlap as in a
-    # training loop, so the pipeline's fill (the first inputs alone on the link) and drain (the
-    # last outputs alone) are spread over the same K steps as the bench line's other figures.
-    steps = args.e2e_steps if args.e2e_steps > 0 else max(5, args.steps)
+    steps = e2e_steps(args)
     for _ in range(steps):
         hs.step(HEADLINE[0])
     for s in hs.streams():

@@ -150,3 +150,18 @@ def test_roofline_by_kind_uses_prequant_runs_and_dtype_peaks():
     assert r["bf16"]["achieved"] == 1000.0 and r["bf16"]["frac"] == 1.0
     assert r["nvfp4"]["achieved"] == 3000.0 and r["nvfp4"]["peak"] == 6000.0 and r["nvfp4"]["frac"] == 0.5
     assert r["fp8_current"]["peak"] == 2000.0 and r["fp8_current"]["frac"] == 0.75
+
+
+def test_e2e_runs_as_many_steps_as_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    old = sys.argv
+    try:
+        for argv, want in ((["bench.py"], None), (["bench.py", "--steps", "20"], 20), (["bench.py", "--steps", "2"], 5),
+                           (["bench.py", "--steps", "20", "--e2e-steps", "3"], 3)):
+            sys.argv = argv
+            args = bench.parse()
+            got = bench.e2e_steps(args)
+            assert got == (want if want is not None else max(5, args.steps))
+    finally:
+        sys.argv = old
